@@ -1,0 +1,426 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks the oracle against exact rational arithmetic (brute force on
+tiny inputs), closed forms and special cases that reduce to a library
+routine, or hand-derived values from the definitions:
+
+* quantizer -- "test_int4_quantized_gemm.py", _packed_with_dense
+  (INT4, group 32, asymmetric min-max);
+* dequant + matmul -- "test_int4_quantized_gemm.py", _dequant_matmul;
+* W4A8 -- "test_int4_quantized_gemm.py", Int4QuantizedGemmPrecisionTest;
+* W8 -- "gpt-fast issue #114", WeightOnlyInt8Linear.forward;
+* packed layout -- this library's layout (the header include/w4q.h).
+"""
+import bisect
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GROUP = 32
+
+# --------------------------------------------------------------------------
+# exact bf16 helpers (independent of the oracle's C code)
+# --------------------------------------------------------------------------
+
+
+def bits_to_float(b: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", (int(b) & 0xFFFF) << 16))[0]
+
+
+def float_to_bits(v: float) -> int:
+    """bf16 bits of a float that is exactly representable in bf16."""
+    u = struct.unpack("<I", struct.pack("<f", v))[0]
+    assert u & 0xFFFF == 0, v
+    return u >> 16
+
+
+_POS = None
+
+
+def positive_bf16():
+    """Every finite positive bf16 as (Fraction value, bits), sorted."""
+    global _POS
+    if _POS is None:
+        _POS = sorted((Fraction(bits_to_float(b)), b) for b in range(1, 0x7F80))
+    return _POS
+
+
+def ru_bf16_brute(v: Fraction) -> int:
+    """Smallest bf16 >= v > 0, by search over every bf16 number."""
+    table = positive_bf16()
+    i = bisect.bisect_left(table, (v, -1))
+    return table[i][1]
+
+
+def clamp15(v):
+    return min(15, max(0, v))
+
+
+def brute_quant_group(wbits):
+    """Exact-rational restatement of the quantizer on one group."""
+    vals = [Fraction(bits_to_float(b)) for b in wbits]
+    mx, mn = max(vals), min(vals)
+    if mx == mn:
+        c = abs(mx)
+        sb = 0x3F80 if c == 0 else ru_bf16_brute(c / 15)
+    else:
+        sb = ru_bf16_brute((mx - mn) / 15)
+    s = Fraction(bits_to_float(sb))
+    z = clamp15(round(-mn / s))          # round(): half to even
+    q = [clamp15(round(v / s) + z) for v in vals]
+    return q, sb, z
+
+
+def quant_rows(groups):
+    """Run the oracle on a list of 32-element groups (one row each)."""
+    W = np.array(groups, dtype=np.uint16).reshape(len(groups), GROUP)
+    q, s, z = oracle.quantize_w4(W, len(groups), GROUP)
+    return q, s, z
+
+
+def randn_bits(shape, seed):
+    return workloads.randn_bf16(shape, seed).view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# quantizer
+# --------------------------------------------------------------------------
+
+
+def test_quantizer_matches_exact_rational_brute_force_on_randn():
+    W = randn_bits((64, 128), seed=5)
+    q, s, z = oracle.quantize_w4(W, 64, 128)
+    for n in range(64):
+        for g in range(128 // GROUP):
+            bq, bs, bz = brute_quant_group(W[n, g * GROUP:(g + 1) * GROUP])
+            assert s[n, g] == bs
+            assert z[n, g] == bz
+            assert list(q[n, g * GROUP:(g + 1) * GROUP]) == bq
+
+
+def _group(values):
+    vals = list(values) + [values[-1]] * (GROUP - len(values))
+    return [float_to_bits(v) for v in vals]
+
+
+ADVERSARIAL = {
+    # range 15 -> s = 1 exactly, z = 1 (odd): w/s = 0.5 must give q = 0 + 1,
+    # not rint(0.5 + 1) = 2 (the zero point is a separately rounded term).
+    "tie_odd_zero": [-1.0, 14.0, 0.5, 1.5, 2.5, -0.5, 3.5, 12.5],
+    # z = 2 (even).
+    "tie_even_zero": [-2.0, 13.0, 0.5, 1.5, 2.5, -1.5, 4.5],
+    "all_zero": [0.0],
+    "negative_zero": [-0.0, 0.0, -0.0],
+    "constant_pos": [3.0],
+    "constant_neg": [-3.0],
+    "same_sign_pos": [1.0, 1.25, 1.5, 2.0],
+    "same_sign_neg": [-1.0, -1.25, -1.5, -2.0],
+    # exact multiples of s = 0.5 around z = 4: dequant is exact.
+    "exact_multiples": [-2.0, 5.5, -1.5, 0.0, 0.5, 3.0, 4.5],
+    "tiny_subnormal_range": [bits_to_float(0x0001), bits_to_float(0x0003)],
+    "huge_range": [bits_to_float(0xFF7F), bits_to_float(0x7F7F), bits_to_float(0x7E96)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(ADVERSARIAL))
+def test_quantizer_adversarial_groups(name):
+    bits = _group(ADVERSARIAL[name])
+    q, s, z = quant_rows([bits])
+    bq, bs, bz = brute_quant_group(bits)
+    assert (int(s[0, 0]), int(z[0, 0]), list(q[0])) == (bs, bz, bq)
+
+
+def test_quantizer_hand_derived_values():
+    # range 15 -> s = 1.0 (bf16 0x3F80), z = rint(1/1) = 1.
+    q, s, z = quant_rows([_group([-1.0, 14.0, 0.5, 1.5, 2.5, -0.5])])
+    assert s[0, 0] == 0x3F80 and z[0, 0] == 1
+    # codes: -1 -> 0, 14 -> 15, 0.5 -> 0+1, 1.5 -> 2+1, 2.5 -> 2+1, -0.5 -> 0+1
+    assert list(q[0, :6]) == [0, 15, 1, 3, 3, 1]
+    # constant 3.0: s = RU_bf16(0.2) = 0.2001953125 (0x3E4D), z = 0, q = 15
+    q, s, z = quant_rows([_group([3.0])])
+    assert s[0, 0] == 0x3E4D and z[0, 0] == 0 and q[0, 0] == 15
+    # constant -3.0: z = 15, q = 0
+    q, s, z = quant_rows([_group([-3.0])])
+    assert s[0, 0] == 0x3E4D and z[0, 0] == 15 and q[0, 0] == 0
+    # all zeros: s = 1.0, z = 0, q = 0 -> dequant exactly 0
+    q, s, z = quant_rows([_group([0.0])])
+    assert s[0, 0] == 0x3F80 and z[0, 0] == 0 and q[0, 0] == 0
+
+
+def test_quantizer_invariants_on_randn():
+    N, K = 512, 1024
+    W = randn_bits((N, K), seed=11)
+    q, s, z = oracle.quantize_w4(W, N, K)
+    assert q.max() <= 15 and z.max() <= 15
+    w = oracle.bf16_bits_to_f64(W).reshape(N, K // GROUP, GROUP)
+    sv = oracle.bf16_bits_to_f64(s)[:, :, None]
+    deq = (q.reshape(N, K // GROUP, GROUP).astype(np.float64) - z[:, :, None]) * sv
+    mx, mn = w.max(axis=2), w.min(axis=2)
+    straddle = (mn <= 0) & (mx >= 0)
+    assert straddle.mean() > 0.99
+    err = np.abs(w - deq)
+    assert np.all(err[straddle] <= sv[straddle] / 2)
+    # s is the least bf16 >= (max - min) / 15 (exact in fp64 for these inputs)
+    rng = (mx - mn) / 15.0
+    assert np.all(sv[:, :, 0] >= rng)
+    prev = oracle.bf16_bits_to_f64(s.astype(np.int64) - 1)
+    assert np.all(prev < rng)
+
+
+def test_dequant_is_q_minus_z_times_s():
+    q = np.array([[0, 15, 7, 8] * 8], dtype=np.uint8)
+    s = np.array([[float_to_bits(0.5)]], dtype=np.uint16)
+    z = np.array([[7]], dtype=np.uint8)
+    d = oracle.dequant_w4(q, s, z)
+    assert list(d[0, :4]) == [-3.5, 4.0, 0.0, 0.5]
+
+
+# --------------------------------------------------------------------------
+# packed layout
+# --------------------------------------------------------------------------
+
+
+def decode_layout(packed, N, K):
+    """Second, vectorised reading of the documented layout (independent of
+    the oracle's scalar code): returns q [N,K], s [N,K/32], z [N,K/32]."""
+    KB, T = K // 256, (N + 15) // 16
+    tiles = packed.reshape(T, KB, 2432)
+    nib = tiles[:, :, :2048].reshape(T, KB, 4, 32, 4, 4)          # sb, lane, word, byte
+    words = nib.astype(np.uint32)
+    words = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)
+    q = np.zeros((T * 16, K), np.uint8)
+    for lane in range(32):
+        r, c = lane // 4, 2 * (lane % 4)
+        for p in range(4):
+            for h in range(2):
+                row = r + 8 * (p & 1)
+                col = c + 8 * (p >> 1) + h
+                vals = (words[:, :, :, lane, :] >> (4 * p + 16 * h)) & 0xF   # T, KB, sb, word
+                for sb in range(4):
+                    for j in range(4):
+                        k = np.arange(KB) * 256 + 64 * sb + 16 * j + col
+                        q[np.arange(T)[:, None] * 16 + row, k[None, :]] = vals[:, :, sb, j]
+    sc = tiles[:, :, 2048:2304].reshape(T, KB, 2, 8, 4, 2, 2)       # ghi, r, glo, half, byte
+    sc = sc[..., 0].astype(np.uint16) | (sc[..., 1].astype(np.uint16) << 8)
+    s = np.zeros((T * 16, K // 32), np.uint16)
+    zr = tiles[:, :, 2304:2432].reshape(T, KB, 8, 8, 2)              # r, g, half
+    z = np.zeros((T * 16, K // 32), np.uint8)
+    for r in range(8):
+        for half in range(2):
+            rows = np.arange(T) * 16 + r + 8 * half
+            for g in range(8):
+                s[rows[:, None], np.arange(KB)[None, :] * 8 + g] = sc[:, :, g // 4, r, g % 4, half]
+                z[rows[:, None], np.arange(KB)[None, :] * 8 + g] = zr[:, :, r, g, half]
+    return q[:N], s[:N], z[:N], q[N:], s[N:], z[N:]
+
+
+def test_packed_size():
+    assert oracle.packed_bytes(256, 768) == 16 * 3 * 2432 == 116736
+    assert oracle.packed_bytes(257, 256) == 17 * 2432
+    assert oracle.packed_bytes(39936, 6656) == 157827072
+    assert oracle.packed_bytes(64, 288) == 0       # K % 256 != 0 is unsupported
+
+
+@pytest.mark.parametrize("N,K", [(16, 256), (257, 512), (40, 768)])
+def test_pack_matches_independent_layout_decoder(N, K):
+    rng = np.random.default_rng(N * 7 + K)
+    q = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    s = rng.integers(0, 0x7F80, (N, K // 32), dtype=np.uint16)
+    z = rng.integers(0, 16, (N, K // 32), dtype=np.uint8)
+    packed = oracle.pack_w4(q, s, z)
+    dq, ds, dz, pq, ps, pz = decode_layout(packed, N, K)
+    np.testing.assert_array_equal(dq, q)
+    np.testing.assert_array_equal(ds, s)
+    np.testing.assert_array_equal(dz, z)
+    assert not pq.any() and not ps.any() and not pz.any()   # padded rows are zero
+    uq, us, uz = oracle.unpack_w4(packed, N, K)
+    np.testing.assert_array_equal(uq, q)
+    np.testing.assert_array_equal(us, s)
+    np.testing.assert_array_equal(uz, z)
+
+
+def test_pack_hand_derived_positions():
+    N, K = 16, 256
+    cases = {  # (n, k) -> (byte, shift) derived by hand from the layout rule
+        (0, 0): (0, 0),      # lane 0, word 0, bit 0
+        (0, 1): (2, 0),      # h = 1 -> bit 16
+        (8, 0): (0, 4),      # p = 1 (row + 8) -> bit 4
+        (0, 8): (1, 0),      # p = 2 (col + 8) -> bit 8
+        (8, 9): (3, 4),      # p = 3, h = 1 -> bit 28
+        (1, 0): (64, 0),     # r = 1 -> lane 4
+        (0, 2): (16, 0),     # c = 2 -> lane 1
+        (0, 16): (4, 0),     # word 1
+        (0, 64): (512, 0),   # sub-block 1
+        (15, 255): (512 * 3 + 16 * 31 + 12 + 3, 4),
+    }
+    for (n, k), (byte, shift) in cases.items():
+        q = np.zeros((N, K), np.uint8)
+        q[n, k] = 0xB
+        packed = oracle.pack_w4(q, np.zeros((N, 8), np.uint16), np.zeros((N, 8), np.uint8))
+        nz = np.flatnonzero(packed)
+        assert list(nz) == [byte], (n, k)
+        assert packed[byte] == 0xB << shift, (n, k)
+    # scale of (row 9, group 5): r = 1, half = 1 -> 2048 + 128 + 16 + 4 + 2
+    s = np.zeros((N, 8), np.uint16)
+    s[9, 5] = 0x1234
+    z = np.zeros((N, 8), np.uint8)
+    z[9, 5] = 7
+    packed = oracle.pack_w4(np.zeros((N, K), np.uint8), s, z)
+    assert packed[2048 + 128 + 16 + 4 + 2] == 0x34 and packed[2048 + 128 + 16 + 4 + 3] == 0x12
+    assert packed[2304 + 16 + 10 + 1] == 7
+    assert np.count_nonzero(packed) == 3
+
+
+# --------------------------------------------------------------------------
+# W4A16 matmul
+# --------------------------------------------------------------------------
+
+
+def _quantized(N, K, seed):
+    W = randn_bits((N, K), seed)
+    q, s, z = oracle.quantize_w4(W, N, K)
+    return W, q, s, z
+
+
+def test_w4a16_exact_rational_brute_force_tiny():
+    N, K, M = 3, 64, 2
+    _, q, s, z = _quantized(N, K, 21)
+    x = randn_bits((M, K), 22)
+    out = oracle.w4a16(x, q, s, z)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(bits_to_float(x[m, k])) *
+                        (int(q[n, k]) - int(z[n, k // 32])) *
+                        Fraction(bits_to_float(s[n, k // 32])) for k in range(K))
+            assert abs(Fraction(out[m, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 60)
+
+
+def test_w4a16_one_hot_selects_a_dequantized_column():
+    N, K = 40, 512
+    _, q, s, z = _quantized(N, K, 31)
+    for k in (0, 31, 32, 255, 256, 511):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80                                  # 1.0
+        out = oracle.w4a16(x, q, s, z)[0]
+        col = (q[:, k].astype(np.float64) - z[:, k // 32]) * oracle.bf16_bits_to_f64(s[:, k // 32])
+        np.testing.assert_array_equal(out, col)
+
+
+def test_w4a16_matches_library_matmul():
+    N, K, M = 256, 768, 4
+    _, q, s, z = _quantized(N, K, 41)
+    x = randn_bits((M, K), 42)
+    ref = oracle.bf16_bits_to_f64(x) @ oracle.dequant_w4(q, s, z).T
+    np.testing.assert_allclose(oracle.w4a16(x, q, s, z), ref, rtol=1e-12, atol=1e-12)
+    # a row window gives the same numbers
+    np.testing.assert_allclose(oracle.w4a16(x, q, s, z, 16, 48), ref[:, 16:48], rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# W4A8
+# --------------------------------------------------------------------------
+
+
+def test_act_quant_hand_derived():
+    K = 8
+    rows = [
+        [127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 3.0, -127.0],    # sx = 1 exactly
+        [0.0] * 8,                                          # all zero -> sx = 0
+        [254.0, 1.0, 3.0, -1.0, 5.0, 0.0, -254.0, 2.0],      # sx = 2: x/2 = .5 ties
+    ]
+    x = np.array([[float_to_bits(v) for v in r] for r in rows], np.uint16)
+    xq, sx = oracle.act_quant(x, K)
+    assert list(sx) == [1.0, 0.0, 2.0]
+    assert list(xq[0]) == [127, 0, 2, 2, 0, -2, 3, -127]
+    assert list(xq[1]) == [0] * 8
+    assert list(xq[2]) == [127, 0, 2, 0, 2, 0, -127, 1]
+
+
+def test_act_quant_matches_exact_rounding_away_from_ties():
+    M, K = 4, 4096
+    x = randn_bits((M, K), 51)
+    xq, sx = oracle.act_quant(x, K)
+    xf = x.astype(np.uint32) << 16
+    xf = xf.view(np.float32)
+    amax = np.abs(xf).max(axis=1)
+    # sx is the fp32 rounding of absmax / 127
+    assert np.array_equal(sx, (amax / np.float32(127)).astype(np.float32))
+    near = 0
+    for m in range(M):
+        s = Fraction(float(sx[m]))
+        for k in range(0, K, 7):
+            v = Fraction(float(xf[m, k])) / s
+            frac = v - int(v)
+            if abs(abs(frac) - Fraction(1, 2)) < Fraction(1, 2 ** 16):
+                near += 1
+                continue
+            assert xq[m, k] == max(-127, min(127, round(v)))
+    assert near < 8
+    assert np.abs(xq).max() == 127
+
+
+def test_w4a8_group_dots_exact_and_bounded():
+    N, K, M = 48, 512, 3
+    _, q, s, z = _quantized(N, K, 61)
+    x = randn_bits((M, K), 62)
+    xq, sx = oracle.act_quant(x, K)
+    D = oracle.w4a8_group_dots(xq, q, z)
+    qq = q.reshape(N, K // 32, 32).astype(np.int64) - z[:, :, None]
+    ref = np.einsum("ngi,mgi->mng", qq, xq.reshape(M, K // 32, 32).astype(np.int64))
+    np.testing.assert_array_equal(D, ref)
+    assert np.abs(D).max() <= 32 * 15 * 127
+
+
+def test_w4a8_reduces_to_w4a16_on_integer_activations():
+    # x integer-valued with max |x| = 127 -> sx = 1 and xq = x exactly, so the
+    # W4A8 result equals the W4A16 result of the same x.
+    N, K, M = 64, 768, 2
+    _, q, s, z = _quantized(N, K, 71)
+    rng = np.random.default_rng(72)
+    xi = rng.integers(-127, 128, (M, K))
+    xi[:, 5] = 127
+    x = np.array([[float_to_bits(float(v)) for v in row] for row in xi], np.uint16)
+    xq, sx = oracle.act_quant(x, K)
+    assert np.all(sx == 1.0) and np.array_equal(xq, xi)
+    np.testing.assert_allclose(oracle.w4a8(xq, sx, q, s, z), oracle.w4a16(x, q, s, z),
+                               rtol=1e-13, atol=1e-9)
+
+
+def test_w4a8_precision_class_against_w4a16_gaussian():
+    # "test_int4_quantized_gemm.py", Int4QuantizedGemmPrecisionTest:
+    # mean |a8 - a16| / mean |a16| <= 0.02 on gaussian activations.
+    N, K = 512, 6656
+    _, q, s, z = _quantized(N, K, 81)
+    for M in (1, 4):
+        x = randn_bits((M, K), 82 + M)
+        xq, sx = oracle.act_quant(x, K)
+        a8 = oracle.w4a8(xq, sx, q, s, z)
+        a16 = oracle.w4a16(x, q, s, z)
+        assert np.abs(a8 - a16).mean() / np.abs(a16).mean() < 0.02
+
+
+# --------------------------------------------------------------------------
+# W8
+# --------------------------------------------------------------------------
+
+
+def test_w8_all_ones_gives_integer_row_sums_times_scale():
+    W, scales, _ = workloads.w8_inputs(N=64, K=512, M=1, seed=91)
+    Wn = W.numpy()
+    x = np.full((1, 512), 0x3F80, np.uint16)
+    out = oracle.w8(x, Wn, scales)
+    sums = Wn.astype(np.int64).sum(axis=1).astype(np.float64)
+    sc = oracle.bf16_bits_to_f64(scales.view(torch.int16).numpy().view(np.uint16))
+    np.testing.assert_array_equal(out[0], sums * sc)
+
+
+def test_w8_matches_library_matmul():
+    W, scales, x = workloads.w8_inputs(N=128, K=1024, M=3, seed=92)
+    ref = (x.double() @ W.double().T * scales.double()).numpy()
+    np.testing.assert_allclose(oracle.w8(x, W.numpy(), scales), ref, rtol=1e-12, atol=1e-9)
