@@ -1,0 +1,53 @@
+// kernels.h -- host-side launchers of the CUDA kernels (internal; the public
+// ABI is w4q.h).  Every launcher only launches: validation happens in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4q {
+
+// --- W4 pack / unpack (pack.cu)
+cudaError_t launch_pack(const void *W, void *packed, int N, int K, cudaStream_t stream);
+cudaError_t launch_unpack(const void *packed, uint8_t *q, void *scale, uint8_t *zero, int N, int K,
+                          cudaStream_t stream);
+
+// --- W4 GEMV / skinny GEMM (gemv_w4.cu)
+
+// Work partition of the W4 kernel: the weight is cut into "tile groups" of
+// 8 row tiles (128 rows) and 256-wide K super-blocks; unit u = g*KB + b.
+// CTA c processes the contiguous units [begin(c), begin(c+1)).
+struct W4Plan {
+    int M, N, K;
+    int KB;         // K / 256
+    int T;          // ceil(N / 16) row tiles
+    int G;          // ceil(T / 8) tile groups
+    int P;          // CTAs
+    int split;      // 0 = balanced (stream-K) ranges, s >= 1 = fixed split
+    int NB;         // n8 blocks of the MMA: 1, 2, 4 or 8
+    bool fold;      // dequantized weight rounded to bf16 (q - z) * s
+    bool fixup;     // some tile group is split over CTAs
+    size_t partial_bytes;  // fp32 partials [P][2][M][128]
+};
+
+enum class W4Mode { A16, A8, A8_DOTS };
+
+// Plan for these sizes (split: -1 = the library's choice, 0 = stream-K,
+// s >= 1 = fixed).  Returns false when the sizes or split are unsupported.
+bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan);
+
+// Workspace bytes for a plan (partials + the W4A8 activation buffers).
+size_t w4_workspace_for(const W4Plan &plan, W4Mode mode);
+
+cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void *packed,
+                      void *out, int32_t *dots, void *workspace, unsigned *err,
+                      cudaStream_t stream);
+
+cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *sx,
+                                cudaStream_t stream);
+
+// --- W8 GEMV (w8.cu)
+cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *out, int M, int N,
+                      int K, int sm_count, unsigned *err, cudaStream_t stream);
+
+}  // namespace w4q

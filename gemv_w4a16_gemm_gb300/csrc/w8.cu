@@ -1,0 +1,234 @@
+// w8.cu -- int8 weight-only GEMV on sm_103a:
+//
+//   out[m,n] = bf16_RN( fp32( sum_k x[m,k] * W[n,k] ) * scales[n] )
+//
+// ("gpt-fast issue #114": WeightOnlyInt8Linear.forward computes
+// F.linear(x, W.to(bf16)) * scales; its fused Inductor reduction streams W
+// once, keeps x resident, accumulates in fp32 and applies the scale at the
+// end.  This kernel is a new GB300 design with the same arithmetic.)
+//
+// Design (one CTA per SM: 16 consumer warps + 1 producer warp):
+//  * CTA c owns a contiguous range of whole rows; those rows are one
+//    contiguous stretch of W, streamed through a shared-memory ring by 1-D
+//    bulk copies (TMA engine, L2 evict-first), RW rows per stage.
+//  * Lane (w, l) owns the 16-byte columns k = 16*(256*ch + 32*w + l) + 0..15
+//    of every row; the matching activations sit in its registers as fp32
+//    for the whole kernel, so each weight byte costs one PRMT (it lands in
+//    the mantissa of 2^23 + 128 + b), one FADD and M FMAs.
+//  * Per row, each warp reduces over its lanes with shuffles and parks the
+//    partial in shared memory; the CTA sums the 16 warp partials in a fixed
+//    order, multiplies by the row scale and rounds once to bf16.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace w4q {
+
+namespace {
+
+constexpr int CWARPS = 16;                  // consumer warps
+constexpr int THREADS = (CWARPS + 1) * 32;  // + producer warp
+constexpr int STAGES = 6;
+constexpr int STAGE_BYTES = 16384;
+constexpr int MAX_ROWS = 64;                // rows per CTA
+constexpr int LANE_SPAN = CWARPS * 32 * 16; // bytes of a row covered per lane chunk
+
+struct W8Params {
+    const int8_t *W;
+    const __nv_bfloat16 *x;
+    const __nv_bfloat16 *scales;
+    __nv_bfloat16 *out;
+    unsigned *err;
+    int N, K, P, RW;
+};
+
+template <int M, int CH>
+__global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    float *red = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);  // [CWARPS][MAX_ROWS][M]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + CWARPS * MAX_ROWS * M);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + STAGES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const int r0 = (int)((long long)c * p.N / p.P), r1 = (int)((long long)(c + 1) * p.N / p.P);
+    const int rows = r1 - r0;
+    const int n_iter = (rows + p.RW - 1) / p.RW;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, CWARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    int issued = 0;
+    if (warp == CWARPS) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            for (int i = 0; i < n_iter; ++i) {
+                const int slot = i % STAGES;
+                if (i >= STAGES &&
+                    !mbar_wait_bounded(empty0 + 8 * slot, (uint32_t)(i / STAGES - 1) & 1)) {
+                    report_error(p.err, ERR_EMPTY_WAIT);
+                    break;
+                }
+                const int ra = r0 + i * p.RW;
+                const int nr = (r1 - ra) < p.RW ? (r1 - ra) : p.RW;
+                const uint32_t bytes = (uint32_t)nr * (uint32_t)p.K;
+                mbar_arrive_expect_tx(full0 + 8 * slot, bytes);
+                bulk_g2s(smem_addr(ring + slot * STAGE_BYTES), p.W + (size_t)ra * p.K, bytes,
+                         full0 + 8 * slot, pol);
+                issued = i + 1;
+            }
+        }
+    } else {
+        // activations of this lane's columns, fp32, for the whole kernel
+        float xr[CH][16][M];
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+            const int k0 = ch * LANE_SPAN + (warp * 32 + lane) * 16;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                if (k0 < p.K) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0);
+                    const uint4 v0 = src[0], v1 = src[1];
+                    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xr[ch][2 * e][m] = bf16lo_to_f32(w[e]);
+                        xr[ch][2 * e + 1][m] = bf16hi_to_f32(w[e]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        xr[ch][e][m] = 0.f;
+                }
+            }
+        }
+        for (int i = 0; i < n_iter; ++i) {
+            const int slot = i % STAGES;
+            if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / STAGES) & 1)) {
+                report_error(p.err, ERR_FULL_WAIT);
+                break;
+            }
+            const int ra = r0 + i * p.RW;
+            const int nr = (r1 - ra) < p.RW ? (r1 - ra) : p.RW;
+            const uint32_t base = smem_addr(ring + slot * STAGE_BYTES);
+            for (int j = 0; j < nr; ++j) {
+                float acc[M];
+#pragma unroll
+                for (int m = 0; m < M; ++m)
+                    acc[m] = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch) {
+                    const int k0 = ch * LANE_SPAN + (warp * 32 + lane) * 16;
+                    if (k0 < p.K) {
+                        const uint4 v = lds128(base + (uint32_t)(j * p.K + k0));
+                        const uint32_t wd[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u,
+                                                v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int bt = 0; bt < 4; ++bt) {
+                                // bytes [u, 0, 0, 0x4B]: 2^23 + u, u = b + 128
+                                const float f =
+                                    __uint_as_float(prmt(wd[q], 0x4B000000u, 0x7440u + bt)) -
+                                    8388736.0f;
+#pragma unroll
+                                for (int m = 0; m < M; ++m)
+                                    acc[m] = fmaf(f, xr[ch][4 * q + bt][m], acc[m]);
+                            }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    float v = acc[m];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0)
+                        red[(warp * MAX_ROWS + (ra - r0 + j)) * M + m] = v;
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8 * slot);
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < rows * M; i += THREADS) {
+        const int row = i / M, m = i % M;
+        float s = 0.f;
+        for (int w = 0; w < CWARPS; ++w)
+            s += red[(w * MAX_ROWS + row) * M + m];
+        const float sc = __bfloat162float(p.scales[r0 + row]);
+        p.out[(size_t)m * p.N + r0 + row] = __float2bfloat16_rn(s * sc);
+    }
+    if (warp == CWARPS && lane == 0) {
+        for (int s = 0; s < STAGES && s < issued; ++s) {
+            const int last_use = (issued - 1 - s) / STAGES;
+            if (!mbar_wait_bounded(full0 + 8 * s, (uint32_t)last_use & 1)) {
+                report_error(p.err, ERR_DRAIN_WAIT);
+                break;
+            }
+        }
+    }
+}
+
+template <int M, int CH>
+cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
+{
+    const int smem = STAGES * STAGE_BYTES + CWARPS * MAX_ROWS * M * 4 + 2 * STAGES * 8;
+    cudaError_t e = cudaFuncSetAttribute(w8_kernel<M, CH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    w8_kernel<M, CH><<<p.P, THREADS, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Supported: 1 <= M <= 4, K % 16 == 0, K <= 16384, M * ceil(K / 8192) <= 4.
+bool w8_supported(int M, int K)
+{
+    if (M < 1 || M > 4 || K < 16 || K % 16 != 0 || K > STAGE_BYTES)
+        return false;
+    const int ch = (K + LANE_SPAN - 1) / LANE_SPAN;
+    return M * ch <= 4;
+}
+
+cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *out, int M, int N,
+                      int K, int sm_count, unsigned *err, cudaStream_t stream)
+{
+    W8Params p;
+    p.W = W;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.scales = static_cast<const __nv_bfloat16 *>(scales);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.err = err;
+    p.N = N;
+    p.K = K;
+    int per_cta = (N + sm_count - 1) / sm_count;
+    if (per_cta > MAX_ROWS)
+        per_cta = MAX_ROWS;
+    p.P = (N + per_cta - 1) / per_cta;
+    int rw = STAGE_BYTES / K;
+    p.RW = rw < 1 ? 1 : (rw > 8 ? 8 : rw);
+    const int ch = (K + LANE_SPAN - 1) / LANE_SPAN;
+    switch (M * 4 + ch) {
+    case 1 * 4 + 1: return launch_t<1, 1>(p, stream);
+    case 1 * 4 + 2: return launch_t<1, 2>(p, stream);
+    case 2 * 4 + 1: return launch_t<2, 1>(p, stream);
+    case 2 * 4 + 2: return launch_t<2, 2>(p, stream);
+    case 3 * 4 + 1: return launch_t<3, 1>(p, stream);
+    case 4 * 4 + 1: return launch_t<4, 1>(p, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace w4q

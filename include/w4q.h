@@ -1,0 +1,214 @@
+/*
+ * w4q.h -- C ABI of the GB300 (sm_103a) weight-only quantized linear layer
+ *
+ *     out[M,N] = x[M,K] . dequant(Wq)[N,K]^T        (decode sizes, M <= 64)
+ *
+ * Three forms, as on the source pages:
+ *   W4A16  INT4 weights, group-wise asymmetric min-max (group 32 along K,
+ *          one scale and one zero point per group), bf16 activations.
+ *          ("test_int4_quantized_gemm.py": _packed_with_dense with
+ *          QuantConfig(bits=4, group_size=32, symmetric=False,
+ *          method="min_max"); the dequant + F.linear reference.)
+ *   W4A8   the same weights, activations quantized per row to symmetric
+ *          int8 inside the call; each group's dot product is an exact
+ *          integer, scaled in fp32.  ("test_int4_quantized_gemm.py": the
+ *          W4A8 bucket kernels and Int4QuantizedGemmPrecisionTest.)
+ *   W8     int8 weights with one bf16 scale per output row.
+ *          ("gpt-fast issue #114": WeightOnlyInt8Linear.forward,
+ *          F.linear(x, W.to(bf16)) * scales, and its fused reduction.)
+ *
+ * Conventions (every entry point):
+ *   - Pointers marked "device" are device pointers owned by the caller; the
+ *     library never frees, retains or allocates memory, and keeps no state
+ *     except a per-device SM-count cache and one device-side error word.
+ *   - Device pointers must be 16-byte aligned, else W4Q_ERR_MISALIGNED.
+ *     Outputs must not alias inputs.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = the legacy default stream) and never synchronize, except
+ *     w4q_device_error.  They may be captured in a CUDA graph.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a status, launches nothing and leaves the
+ *     outputs untouched.  A failed launch returns W4Q_ERR_CUDA.  No call
+ *     aborts or exits the process.
+ *   - Results are bitwise reproducible for a given (M, N, K, split, device
+ *     SM count): reductions run in a fixed order, with no floating-point
+ *     atomics.  ("test_int4_quantized_gemm.py": repeated calls and CUDA
+ *     graph replay are bitwise equal to eager.)
+ *   - W4 shapes: 1 <= M <= 64, N >= 1, K a positive multiple of 256
+ *     ("test_int4_quantized_gemm.py", Int4QuantizedGemmLegalityTest: K must
+ *     be a multiple of 256), group == 32 (the only supported group size).
+ *   - Non-finite inputs give unspecified (but memory-safe) outputs.
+ *
+ * Packed W4 layout (this library's own; the pages' storage is prior art):
+ *   Rows are grouped in tiles of 16 (N is padded up to a multiple of 16 with
+ *   all-zero rows), K in super-blocks of 256 (8 groups).  Tile (t, b),
+ *   t < ceil(N/16), b < K/256, is 2432 bytes at offset (t*(K/256) + b)*2432:
+ *     [0, 2048)     4-bit codes q.  Sub-block sb = kk/64 (kk = k - 256b) at
+ *                   512*sb; "lane" l in 0..31 at +16*l; little-endian 32-bit
+ *                   word j = (kk%64)/16 at +4*j.  Inside word j, with
+ *                   r = l/4 and c = 2*(l%4), the nibble at bit 4p + 16h
+ *                   (p in 0..3, h in 0..1) is the code of row
+ *                   16t + r + 8*(p&1) and column 256b + 64sb + 16j + c +
+ *                   8*(p>>1) + h.  (One 16-byte lane chunk is exactly the
+ *                   four bf16 A fragments of an m16n8k16 MMA for that lane.)
+ *     [2048, 2304)  bf16 scales s.  The pair (s[16t+r][8b+g],
+ *                   s[16t+r+8][8b+g]) is at 2048 + 128*(g/4) + 16*r +
+ *                   4*(g%4), row r first (r in 0..7, g in 0..7).
+ *     [2304, 2432)  u8 zero points z, the pair (z[16t+r][8b+g],
+ *                   z[16t+r+8][8b+g]) at 2304 + 16*r + 2*g.
+ *   Every field starts on a 16-byte boundary, so each CTA streams whole
+ *   tiles with 1-D bulk copies and each lane reads 16-byte chunks.
+ *
+ * Quantizer (w4_pack_weights), per row n and group g of 32 columns, with
+ * max/min over the group:
+ *   s = the smallest bf16 >= fl64(fl64(max - min) / 15)   (round up, so
+ *       |w - dequant| <= s/2 whenever min <= 0 <= max);
+ *       a constant group c uses s = RU_bf16(|c| / 15), or 1.0 if c == 0;
+ *   z = clamp(rint(-min / s), 0, 15);  q = clamp(rint(w / s) + z, 0, 15)
+ *       (rint = round half to even; z and q use the stored bf16 s);
+ *   dequant(q) = (q - z) * s.
+ */
+#ifndef W4Q_H
+#define W4Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4Q_OK = 0,
+    W4Q_ERR_INVALID_ARG = 1,  /* null pointer, negative or zero size      */
+    W4Q_ERR_UNSUPPORTED = 2,  /* M, K, group or split outside the ranges  */
+    W4Q_ERR_MISALIGNED = 3,   /* a device pointer not 16-byte aligned     */
+    W4Q_ERR_WORKSPACE = 4,    /* workspace missing or too small           */
+    W4Q_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed     */
+    W4Q_ERR_DEVICE = 6        /* a kernel reported a bounded-wait timeout */
+} w4q_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *w4q_status_string(int status);
+
+/* ---------------------------------------------------------------- W4 --- */
+
+/* Bytes of the packed W4 buffer for an [N,K] weight: ceil(N/16)*(K/256)*2432.
+ * Returns 0 when (N, K, group) is unsupported. */
+size_t w4_packed_bytes(int64_t N, int64_t K, int group);
+
+/* Quantize a bf16 weight and write it in the packed layout above.
+ *   W_bf16  device, bf16 [N,K] row-major (read only)
+ *   packed  device, w4_packed_bytes(N,K,group) bytes (written, fully)
+ * Defined by "test_int4_quantized_gemm.py", _packed_with_dense (INT4,
+ * group 32, asymmetric min-max); the rounding choices are in the header
+ * comment.  One launch; no workspace. */
+int w4_pack_weights(const void *W_bf16, int64_t N, int64_t K, int group,
+                    void *packed, void *stream);
+
+/* Inverse view of the packed buffer, for tests and tools.
+ *   q      device, u8 [N,K], one code per byte (written)
+ *   scale  device, bf16 [N,K/32] (written)
+ *   zero   device, u8 [N,K/32] (written)
+ * Padding rows are not written. */
+int w4_unpack_weights(const void *packed, int64_t N, int64_t K, int group,
+                      uint8_t *q, void *scale_bf16, uint8_t *zero,
+                      void *stream);
+
+/* Workspace bytes needed by w4a16_gemm and w4a8_gemm for these sizes on the
+ * current device with the library's own split choice (0 if none is needed;
+ * w4a8_gemm always needs some).  One buffer of this size serves both. */
+size_t w4_workspace_bytes(int64_t M, int64_t N, int64_t K, int group);
+
+/* Same, for an explicit split_k (see w4a16_gemm_split); 0 if unsupported. */
+size_t w4_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int group,
+                                int split_k);
+
+/* The split the library picks for these sizes on the current device:
+ * 0 = balanced stream-K partition over all SMs, s >= 1 = fixed K split. */
+int w4_split_choice(int64_t M, int64_t N, int64_t K, int group);
+
+/* Number of kernels one w4a16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1) call
+ * with these sizes launches on the current device with the library's own
+ * split choice: the main kernel, plus the W4A8 activation quantizer, plus
+ * the split-K fixup when a tile group is shared by several CTAs.  -1 when
+ * the sizes are unsupported. */
+int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
+
+/* out = x . dequant(packed)^T, W4A16.
+ *   x          device, bf16 [M,K] row-major
+ *   packed     device, from w4_pack_weights(N, K)
+ *   out        device, bf16 [M,N] row-major (written)
+ *   workspace  device scratch of >= w4_workspace_bytes(M,N,K,group) bytes
+ *              (may be NULL when that is 0); contents are clobbered.
+ * Accumulates in fp32: per group, sum_k (q - z) * x exactly in the tensor
+ * core, then acc += s * sum; for M > 16 the dequantized weight is rounded
+ * once to bf16 ((q - z) * s) and accumulated over all of K.
+ * out = bf16_RN(acc).  Defined by "test_int4_quantized_gemm.py", the
+ * dequant + F.linear reference. */
+int w4a16_gemm(const void *x_bf16, const void *packed, void *out_bf16,
+               int64_t M, int64_t N, int64_t K, int group, void *workspace,
+               size_t workspace_bytes, void *stream);
+
+/* As w4a16_gemm with an explicit K partition: split_k = s >= 1 splits each
+ * 16*8-row tile group's K range into s contiguous parts of whole 256-wide
+ * super-blocks (legal iff s <= K/256, "test_int4_quantized_gemm.py",
+ * Int4QuantizedGemmRulesTest: one 256-wide K tile per split), partials are
+ * summed in fixed order; split_k = 0 is the balanced stream-K partition the
+ * library uses by default.  Illegal s returns W4Q_ERR_UNSUPPORTED. */
+int w4a16_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
+                     int64_t M, int64_t N, int64_t K, int group, int split_k,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* out = x . dequant(packed)^T, W4A8: per row m, sx = fp32(max|x| / 127),
+ * xq = clamp(rint(x / sx), -127, 127) in IEEE fp32 (xq = 0 when max|x| = 0);
+ * per group D = sum_k (q - z) * xq, an exact integer (|D| <= 60960);
+ * acc = sum_g s_g * D_g in fp32; out = bf16_RN(sx * acc).
+ * Arguments as w4a16_gemm; the workspace is required (it holds xq and sx). */
+int w4a8_gemm(const void *x_bf16, const void *packed, void *out_bf16,
+              int64_t M, int64_t N, int64_t K, int group, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+int w4a8_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
+                    int64_t M, int64_t N, int64_t K, int group, int split_k,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* The W4A8 activation quantizer alone (same device code as w4a8_gemm).
+ *   xq  device, int8 [M,K] (written);  sx  device, f32 [M] (written). */
+int w4a8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq,
+                      float *sx, void *stream);
+
+/* The exact W4A8 group dot products, for bit-exact checks.
+ *   D          device, int32 [M][N][K/32] (written)
+ *   workspace  device, >= w4_workspace_bytes(M,N,K,group) bytes
+ * Uses the same activation quantizer and the same tensor-core group dot as
+ * w4a8_gemm. */
+int w4a8_group_dots(const void *x_bf16, const void *packed, int64_t M,
+                    int64_t N, int64_t K, int group, int32_t *D,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------- W8 --- */
+
+/* out[m,n] = bf16_RN(fp32(sum_k x[m,k] * W[n,k]) * scales[n]), one rounding
+ * ("gpt-fast issue #114": WeightOnlyInt8Linear.forward and the fused
+ * int8 -> fp32 reduction).
+ *   x       device, bf16 [M,K] row-major, 1 <= M <= 4
+ *   W       device, int8 [N,K] row-major, K a positive multiple of 16
+ *   scales  device, bf16 [N]
+ *   out     device, bf16 [M,N] (written)
+ * No workspace. */
+int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16,
+            void *out_bf16, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* ------------------------------------------------------------ status --- */
+
+/* Read and clear the device-side error word of the current device (set by
+ * a kernel whose bounded wait on a barrier ran out).  Synchronizes the
+ * device.  *code receives the word (0 = no error). */
+int w4q_device_error(uint32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4Q_H */

@@ -18,3 +18,12 @@ def cuda():
     if not torch.cuda.is_available():
         pytest.skip("CUDA GPU required")
     return torch.device("cuda:0")
+
+
+def pytest_sessionstart(session):
+    # (Re)build the CUDA library and the CPU oracle when their sources are
+    # newer than the binaries; a no-op when they are current.
+    from gemv_w4a16_gemm_gb300 import build as libbuild
+    import oracle
+    libbuild.build()
+    oracle.build()

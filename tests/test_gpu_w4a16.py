@@ -1,0 +1,137 @@
+"""W4A16 on the GPU vs the fp64 oracle ("test_int4_quantized_gemm.py": the
+dequant + F.linear reference, every bucket on small and model shapes, the
+tail shape N = 257, every legal split, dynamic M)."""
+import pytest
+import torch
+
+import oracle
+import workloads
+from gemv_w4a16_gemm_gb300 import w4q
+from helpers import assert_close, quantized
+
+pytestmark = pytest.mark.gpu
+
+BUCKETS = (1, 2, 3, 4, 8, 16, 32, 64)
+
+
+def _run(cuda, N, K, Ms, seed_w=None, split_k=None):
+    W, q, s, z = quantized(N, K, seed_w)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in Ms:
+        x = workloads.activation(M, K, seed=workloads.x_seed(N, K, M))
+        out = w4q.w4a16_gemm(x.to(cuda), packed, N, K, split_k=split_k)
+        assert out.shape == (M, N) and out.dtype == torch.bfloat16
+        assert_close(out, oracle.w4a16(x, q, s, z), "N=%d K=%d M=%d split=%s" % (N, K, M, split_k))
+
+
+@pytest.mark.parametrize("N,K", workloads.SMALL_SHAPES + ((257, 256), (257, 512), (16, 256), (1, 256)))
+def test_small_shapes_every_bucket(cuda, N, K):
+    _run(cuda, N, K, BUCKETS, seed_w=N + K)
+
+
+def test_tiny_workload(cuda):
+    W, x = workloads.tiny_w4a16()
+    N, K = W.shape
+    q, s, z = oracle.quantize_w4(W, N, K)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    assert_close(w4q.w4a16_gemm(x.to(cuda), packed, N, K), oracle.w4a16(x, q, s, z), "tiny")
+
+
+@pytest.mark.parametrize("N,K", workloads.W4A16_GEMV_SHAPES)
+def test_gemv_model_shapes_full(cuda, N, K):
+    _run(cuda, N, K, workloads.W4A16_GEMV_MS)
+
+
+@pytest.mark.parametrize("N,K", workloads.TC_SHAPES)
+def test_skinny_gemm_shapes(cuda, N, K):
+    # M = 16 / 64 on the full shapes; the 39936 x 6656 M = 64 oracle is the
+    # slowest case (about 17 G multiply-adds), so outputs are compared on a
+    # window of rows there and in full elsewhere.
+    W, q, s, z = quantized(N, K)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in workloads.TC_MS:
+        x = workloads.activation(M, K, seed=workloads.x_seed(N, K, M))
+        out = w4q.w4a16_gemm(x.to(cuda), packed, N, K)
+        if N * K * M > 6e9:
+            for a, b in ((0, 256), (N // 2, N // 2 + 128), (N - 200, N)):
+                assert_close(out[:, a:b], oracle.w4a16(x, q, s, z, a, b), "M=%d rows %d:%d" % (M, a, b))
+        else:
+            assert_close(out, oracle.w4a16(x, q, s, z), "N=%d K=%d M=%d" % (N, K, M))
+
+
+def test_every_legal_split_matches(cuda):
+    # "test_int4_quantized_gemm.py", test_every_split_matches_dequant_matmul
+    N, K = 256, 4096
+    W, q, s, z = quantized(N, K, seed=91)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in (1, 2, 3, 4, 16):
+        x = workloads.activation(M, K, seed=100 + M)
+        ref = oracle.w4a16(x, q, s, z)
+        for split in (0, 1, 2, 3, 4, 5, 7, 8, 16):
+            assert_close(w4q.w4a16_gemm(x.to(cuda), packed, N, K, split_k=split), ref,
+                         "M=%d split=%d" % (M, split))
+
+
+def test_illegal_split_is_rejected(cuda):
+    N, K = 256, 768
+    W = workloads.w4_weight(N, K, seed=0)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    x = torch.randn(1, K, dtype=torch.bfloat16, device=cuda)
+    out = torch.full((1, N), 7.0, dtype=torch.bfloat16, device=cuda)
+    with pytest.raises(w4q.W4QError) as e:
+        w4q.w4a16_gemm(x, packed, N, K, split_k=4, out=out)
+    assert e.value.status == 2
+    assert torch.all(out == 7.0)   # nothing launched, output untouched
+
+
+def test_every_runtime_m_up_to_64(cuda):
+    # one compiled kernel per n8 width serves every M below it (rows masked)
+    N, K = 300, 512
+    W, q, s, z = quantized(N, K, seed=5)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in range(1, 65):
+        x = workloads.activation(M, K, seed=M)
+        assert_close(w4q.w4a16_gemm(x.to(cuda), packed, N, K), oracle.w4a16(x, q, s, z), "M=%d" % M)
+
+
+def test_workspace_too_small_is_rejected(cuda):
+    # w4_workspace_bytes covers both W4A16 and W4A8 (the larger, with the
+    # int8 activation buffers); a buffer 16 bytes short fails W4A8, and a
+    # 16-byte buffer fails W4A16 when it needs split-K partials.
+    N, K, M = 8448, 6656, 4
+    need = w4q.workspace_bytes(M, N, K)
+    assert need > 0
+    W = workloads.w4_weight(N, K)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    x = torch.randn(M, K, dtype=torch.bfloat16, device=cuda)
+    out = torch.full((M, N), 3.0, dtype=torch.bfloat16, device=cuda)
+    small = torch.empty(need - 16, dtype=torch.uint8, device=cuda)
+    with pytest.raises(w4q.W4QError) as e:
+        w4q.w4a8_gemm(x, packed, N, K, workspace=small, out=out)
+    assert e.value.status == 4
+    if w4q.kernel_launches(M, N, K) > 1:          # a fixup: partials needed
+        with pytest.raises(w4q.W4QError) as e:
+            w4q.w4a16_gemm(x, packed, N, K, workspace=small[:16], out=out)
+        assert e.value.status == 4
+    assert torch.all(out == 3.0)
+
+
+def test_misaligned_pointer_is_rejected(cuda):
+    N, K = 64, 256
+    W = workloads.w4_weight(N, K, seed=1)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    xbuf = torch.zeros(2 * K + 8, dtype=torch.bfloat16, device=cuda)
+    x = xbuf[1:1 + K].view(1, K)      # 2-byte offset
+    with pytest.raises(w4q.W4QError) as e:
+        w4q.w4a16_gemm(x, packed, N, K)
+    assert e.value.status == 3
+
+
+def test_zero_activation_gives_zero(cuda):
+    N, K = 257, 512
+    W = workloads.w4_weight(N, K, seed=2)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in (1, 4, 64):
+        out = w4q.w4a16_gemm(torch.zeros(M, K, dtype=torch.bfloat16, device=cuda), packed, N, K)
+        assert torch.all(out == 0)
+    assert w4q.device_error() == 0
