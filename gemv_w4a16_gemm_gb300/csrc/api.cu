@@ -143,7 +143,7 @@ size_t w4_packed_bytes(int64_t N, int64_t K, int group)
 {
     if (check_w4_shape(1, N, K, group) != W4Q_OK)
         return 0;
-    return (size_t)((N + 15) / 16) * (size_t)(K / 256) * 2432u;
+    return (size_t)((N + 127) / 128) * 8u * (size_t)(K / 256) * 2432u;
 }
 
 int w4_pack_weights(const void *W_bf16, int64_t N, int64_t K, int group, void *packed,
@@ -212,7 +212,8 @@ int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8)
     w4q::W4Plan plan;
     if (!w4q::w4_plan((int)M, (int)N, (int)K, -1, sm_count(dev), mode, &plan))
         return -1;
-    return 1 + (w4a8 ? 1 : 0) + (plan.fixup ? 1 : 0);
+    (void)plan;
+    return 2;  // the activation preparation (and counter reset), then the main kernel
 }
 
 int w4a16_gemm(const void *x_bf16, const void *packed, void *out_bf16, int64_t M, int64_t N,

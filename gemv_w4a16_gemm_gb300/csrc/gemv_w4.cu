@@ -6,33 +6,53 @@
 // bucket kernels and the W4A16 tile kernels; this is a new design for GB300,
 // not their code.)
 //
-// Design (one CTA = 8 consumer warps + 1 producer warp):
-//  * The weight is read once, as whole 2432-byte packed tiles (16 rows x 256
-//    K, codes + scales + zeros), by 1-D bulk copies (TMA engine) into a
-//    multi-stage shared-memory ring guarded by mbarriers; the activation
-//    chunk of the same 256 K rides along in the same stage.  Weights carry
-//    an L2 evict-first hint, activations evict-last.
-//  * Consumer warp w owns row tile w of the CTA's 128-row tile group.  A
-//    lane's 16 bytes of a sub-block are exactly its four bf16 A fragments of
-//    four m16n8k16 MMAs (the layout is built for this), so dequant is two
-//    ALU ops per pair of codes: LOP3 puts a nibble into the mantissa of
-//    bf16 128.0, and one packed bf16 subtract of (128 + z) leaves the exact
-//    integer q - z.  The tensor core then sums (q - z) * x over each group
-//    of 32 exactly; the fp32 group sum is scaled by s and accumulated
-//    (M <= 16).  For M > 16 the scaled weight (q - z) * s is rounded to bf16
-//    once and the MMA accumulates over all of K (per-group fp32 scaling
-//    would cost more ALU than the tensor core saves).
-//  * W4A8: activations are int8 values held as exact bf16 integers, so the
-//    per-group MMA sum (|D| <= 60960 < 2^24) is the exact integer dot; the
-//    same kernel then scales by s in fp32 and by the row scale at the end.
-//  * Work partition: units (tile group, 256-K super-block) are split into
-//    P contiguous ranges, one per CTA (balanced "stream-K" ranges over all
-//    SM slots by default, or a fixed split of each group's K).  A group that
-//    one CTA covers entirely is written directly; the other groups write
-//    fp32 partials that a fixup kernel sums in CTA order (deterministic, no
-//    atomics).  The fixup is launched with programmatic dependent launch.
-//  * Every wait is bounded (one second of %globaltimer); on expiry the
-//    kernel sets a bit in the error word, drains its copies and returns.
+// Two launches per call:
+//  1. act_prep (one CTA per activation row) prepares the activation operand
+//     in the workspace, super-block-major ([K/256][M][256 + 8 pad] bf16 and
+//     [K/256][M][8] fp32, so one bulk copy moves a stage's rows), and zeroes
+//     the split-K counters:
+//       W4A16:  x' = x * 2^sigma, with an extra 2^-4 on the upper eight
+//               columns of every 16-column step (sigma from max|x|, so x'
+//               stays finite); X'[g] = 2^(sigma-133) * sum_{k in g} x_k;
+//               out scale 2^(133 - sigma).
+//       W4A8:   sx = fp32(max|x| / 127), xq = clamp(rint(fp32(x / sx))),
+//               x' = xq * 2^121 (2^117 on upper halves), X'[g] =
+//               2^-12 * sum xq (exact), out scale sx * 2^12.
+//  2. w4_kernel (launched with programmatic dependent launch, so it starts
+//     streaming weights while act_prep runs): one CTA = 8 consumer warps +
+//     1 producer warp.
+//       * The weight is read once: each stage is one 19456-byte bulk copy
+//         (TMA engine) of the 8 packed tiles (16 rows x 256 K: codes,
+//         scales, zeros) of a 128-row group, plus one copy each of the
+//         matching x' rows and X' slice, into a multi-stage shared-memory
+//         ring guarded by mbarriers (three copies per stage: the TMA issue
+//         rate, about one copy per 70 SM cycles, is a real limit).
+//         Weights carry an L2 evict-first hint, activations evict-last.
+//       * Consumer warp w owns row tile w of the CTA's 128-row tile group.
+//         A lane's 16 bytes of a sub-block hold its A fragments of four
+//         m16n8k16 MMAs; masking a word with 0x000F000F / 0x00F000F0 turns
+//         its codes into the bf16 numbers q * 2^-133 / q * 2^-129 (exact
+//         subnormals / first normals), so dequant is one shift and four ANDs
+//         per eight codes.  The 2^4 between the two masks is what the 2^-4
+//         on the upper columns of x' undoes.  The tensor core then sums
+//         q * x' over each group of 32; the zero point enters as
+//         D - z * X'[g] and the scale as acc += s * (D - z * X'[g]) (fp32).
+//         For W4A8 every product and partial sum is an exact multiple of
+//         2^-12 below 2^12, so the group dot is the exact integer dot.
+//       * For W4A16 at M > 16 the scaled weight (q - z) * s is rounded once
+//         to bf16 (codes via 128-offset bf16 arithmetic) and the MMA
+//         accumulates over all of K on the unscaled x: per-group fp32
+//         scaling would cost more ALU than the tensor core saves.
+//       * Work partition: units (tile group, 256-K super-block) are split
+//         into P contiguous ranges, one per CTA (balanced "stream-K" ranges
+//         over all SM slots by default, or a fixed split of each group's K).
+//         A group that one CTA covers entirely is written directly.  For the
+//         other groups every contributing warp writes its fp32 partial and
+//         bumps a per-row-tile counter; the warp that bumps it last sums the
+//         partials in CTA order (deterministic, no floating-point atomics,
+//         no waiting on other CTAs) and writes the outputs.
+//       * Every wait is bounded (one second of %globaltimer); on expiry the
+//         kernel sets a bit in the error word, drains its copies and returns.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -42,16 +62,20 @@ namespace {
 
 constexpr int TILE_BYTES = 2432;
 constexpr int WARPS = 8;                   // consumer warps = row tiles per tile group
+constexpr int GROUP_ROWS = WARPS * 16;     // rows of one tile group
 constexpr int THREADS = (WARPS + 1) * 32;  // + one producer warp
 constexpr int XROW = 512 + 16;             // one activation row's 256-K chunk, padded
+constexpr int SROW = 32;                   // one activation row's 8 group sums (fp32)
 
 struct Params {
     const uint8_t *packed;
-    const __nv_bfloat16 *x;  // bf16 [M][K]; W4A8: the int8 activations as bf16
-    const float *sx;         // W4A8 per-row activation scales
+    const __nv_bfloat16 *x;  // bf16 [K/256][M][264]: x' (prepared) or, when folding, x
+    const float *xsum;       // fp32 [K/256][M][8]: X' (not used when folding)
+    const float *oscale;     // fp32 [M]: output scale per row
     __nv_bfloat16 *out;      // bf16 [M][N]
     int32_t *dots;           // group-dot export: int32 [M][N][K/32]
-    float *partial;          // fp32 [P][2][M][128]
+    float *partial;          // fp32 [P][2][M][GROUP_ROWS]
+    unsigned *counters;      // [G][WARPS] arrivals per row tile (zeroed by act_prep)
     unsigned *err;
     int M, N, K, KB, T, G, P, split;
     long long U;
@@ -65,26 +89,52 @@ __host__ __device__ __forceinline__ long long range_begin(const Params &p, int c
     return (long long)g * p.KB + (long long)j * p.KB / p.split;
 }
 
-template <int NB>
+// The CTA whose range holds unit u (the largest c with range_begin(c) <= u).
+__device__ __forceinline__ int range_owner(const Params &p, long long u)
+{
+    if (p.split == 0)
+        return (int)(((u + 1) * p.P - 1) / p.U);
+    const int g = (int)(u / p.KB), b = (int)(u % p.KB);
+    return g * p.split + (int)(((long long)(b + 1) * p.split - 1) / p.KB);
+}
+
+// The dequantized weight is folded into bf16 for W4A16 at M > 16 (NB >= 4).
+template <int NB, W4Mode MODE>
+__host__ __device__ constexpr bool fold_for()
+{
+    return MODE == W4Mode::A16 && NB >= 4;
+}
+
+template <int NB, W4Mode MODE>
+__host__ __device__ constexpr int stage_bytes()
+{
+    return WARPS * TILE_BYTES + NB * 8 * XROW + (fold_for<NB, MODE>() ? 0 : NB * 8 * SROW);
+}
+
+template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int stages_for()
 {
-    return NB <= 2 ? 4 : (NB == 4 ? 3 : 4);
+    int s = NB == 1 ? 4 : (NB == 4 ? 3 : 4);
+    while (s > 2 && s * stage_bytes<NB, MODE>() + 16 * s > 227 * 1024)
+        --s;
+    return s;
 }
 
-template <int NB>
+template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int smem_for()
 {
-    return stages_for<NB>() * (WARPS * TILE_BYTES + NB * 8 * XROW) + 2 * stages_for<NB>() * 8;
+    return stages_for<NB, MODE>() * stage_bytes<NB, MODE>() + 2 * stages_for<NB, MODE>() * 8;
 }
 
-// One stage = one 16 x 256 tile for this warp: 4 sub-blocks of 64 K (two
-// groups each), 4 k16 steps per sub-block.
+// One stage: this warp's 16 x 256 tile, 4 sub-blocks of 64 K (two groups
+// each), 4 k16 steps per sub-block.  xbase: the stage's activation rows;
+// sbase: the stage's group sums (unused when folding).
 template <int NB, bool FOLD, bool DOTS>
-__device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, int lane,
-                                              float (&acc)[NB][4], const Params &p, int tile,
-                                              int b)
+__device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, uint32_t sbase,
+                                              int lane, float (&acc)[NB][4], const Params &p,
+                                              int tile, int b)
 {
-    const int r = lane >> 2;
+    const int r = lane >> 2, c2 = 2 * (lane & 3);
     const uint4 sc0 = lds128(wbase + 2048 + 16 * r);
     const uint4 sc1 = lds128(wbase + 2048 + 128 + 16 * r);
     const uint4 zz = lds128(wbase + 2304 + 16 * r);
@@ -93,6 +143,26 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, in
     // ldmatrix.x4 row addresses: matrix lane>>3 = (step +lane>>4, k half (lane>>3)&1)
     const uint32_t xlane = xbase + (lane & 7) * XROW + 32 * (lane >> 4) + 16 * ((lane >> 3) & 1);
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+
+    // group sums X' of this lane's two output columns, per n8 block
+    float xs[NB][2][8];
+    if (!FOLD) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t a = sbase + (nb * 8 + c2 + e) * SROW;
+                const uint4 v0 = lds128(a), v1 = lds128(a + 16);
+                xs[nb][e][0] = __uint_as_float(v0.x);
+                xs[nb][e][1] = __uint_as_float(v0.y);
+                xs[nb][e][2] = __uint_as_float(v0.z);
+                xs[nb][e][3] = __uint_as_float(v0.w);
+                xs[nb][e][4] = __uint_as_float(v1.x);
+                xs[nb][e][5] = __uint_as_float(v1.y);
+                xs[nb][e][6] = __uint_as_float(v1.z);
+                xs[nb][e][7] = __uint_as_float(v1.w);
+            }
+    }
 
 #pragma unroll
     for (int sbk = 0; sbk < 4; ++sbk) {
@@ -108,48 +178,49 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, in
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
             const int g = 2 * sbk + gi;
-            // (128 + z) in both bf16 halves, rows r and r + 8
             const uint32_t zsrc = zw[g >> 1];
-            const uint32_t zb = (uint32_t)((2 * g) & 3);
-            const uint32_t zr = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * zb);
-            const uint32_t zr8 = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * (zb + 1));
+            const uint32_t zb = (uint32_t)((2 * g) & 3);  // byte of z[r][g]; z[r+8][g] follows
             const uint32_t sp = scw[g];
-            uint32_t s2r = 0, s2r8 = 0;
             if (FOLD) {
-                s2r = prmt(sp, sp, 0x1010u);
-                s2r8 = prmt(sp, sp, 0x3232u);
-            }
-            float d[NB][4];
+                // (128 + z) in both bf16 halves, rows r and r + 8
+                const uint32_t zr = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * zb);
+                const uint32_t zr8 = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * (zb + 1));
+                const uint32_t s2r = prmt(sp, sp, 0x1010u), s2r8 = prmt(sp, sp, 0x3232u);
 #pragma unroll
-            for (int st = 0; st < 2; ++st) {
-                const uint32_t w = wv[2 * gi + st];
-                uint32_t a[4];
-                a[0] = bf16x2_sub(and_or(w, 0x000F000Fu, 0x43004300u), zr);
-                a[1] = bf16x2_sub(and_or(w >> 4, 0x000F000Fu, 0x43004300u), zr8);
-                a[2] = bf16x2_sub(and_or(w >> 8, 0x000F000Fu, 0x43004300u), zr);
-                a[3] = bf16x2_sub(and_or(w >> 12, 0x000F000Fu, 0x43004300u), zr8);
-                if (FOLD) {
-                    a[0] = bf16x2_mul(a[0], s2r);
-                    a[1] = bf16x2_mul(a[1], s2r8);
-                    a[2] = bf16x2_mul(a[2], s2r);
-                    a[3] = bf16x2_mul(a[3], s2r8);
+                for (int st = 0; st < 2; ++st) {
+                    const uint32_t w = wv[2 * gi + st];
+                    uint32_t a[4];  // rows r, r+8 x cols c, c+8 (bits 0, 8, 4, 12)
+                    a[0] = bf16x2_mul(bf16x2_sub(and_or(w, 0x000F000Fu, 0x43004300u), zr), s2r);
+                    a[1] = bf16x2_mul(bf16x2_sub(and_or(w >> 8, 0x000F000Fu, 0x43004300u), zr8), s2r8);
+                    a[2] = bf16x2_mul(bf16x2_sub(and_or(w >> 4, 0x000F000Fu, 0x43004300u), zr), s2r);
+                    a[3] = bf16x2_mul(bf16x2_sub(and_or(w >> 12, 0x000F000Fu, 0x43004300u), zr8), s2r8);
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb)
-                        mma_bf16(acc[nb], a, bf[nb][2 * gi + st][0], bf[nb][2 * gi + st][1],
-                                 acc[nb]);
-                } else {
+                        mma_bf16(acc[nb], a, bf[nb][2 * gi + st][0], bf[nb][2 * gi + st][1], acc[nb]);
+                }
+            } else {
+                float d[NB][4];
+#pragma unroll
+                for (int st = 0; st < 2; ++st) {
+                    const uint32_t w = wv[2 * gi + st], t = w >> 8;
+                    uint32_t a[4];  // q * 2^-133 (low nibbles), q * 2^-129 (high nibbles)
+                    a[0] = w & 0x000F000Fu;
+                    a[1] = t & 0x000F000Fu;
+                    a[2] = w & 0x00F000F0u;
+                    a[3] = t & 0x00F000F0u;
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
                         if (st == 0)
-                            mma_bf16(d[nb], a, bf[nb][0 + 2 * gi][0], bf[nb][0 + 2 * gi][1], zero4);
+                            mma_bf16(d[nb], a, bf[nb][2 * gi][0], bf[nb][2 * gi][1], zero4);
                         else
-                            mma_bf16(d[nb], a, bf[nb][1 + 2 * gi][0], bf[nb][1 + 2 * gi][1], d[nb]);
+                            mma_bf16(d[nb], a, bf[nb][2 * gi + 1][0], bf[nb][2 * gi + 1][1], d[nb]);
                     }
                 }
-            }
-            if (!FOLD) {
+                // -z as fp32: bytes [z, 0, 0, 0x4B] = 2^23 + z
+                const float nzr = 8388608.0f - __uint_as_float(prmt(zsrc, 0x4B000000u, 0x7440u + zb));
+                const float nzr8 =
+                    8388608.0f - __uint_as_float(prmt(zsrc, 0x4B000000u, 0x7440u + zb + 1));
                 if (DOTS) {
-                    const int c2 = 2 * (lane & 3);
                     const int G = p.K / 32, gg = b * 8 + g;
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb)
@@ -157,17 +228,18 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, in
                         for (int e = 0; e < 4; ++e) {
                             const int m = nb * 8 + c2 + (e & 1);
                             const int n = tile * 16 + r + 8 * (e >> 1);
+                            const float dg = fmaf((e >> 1) ? nzr8 : nzr, xs[nb][e & 1][g], d[nb][e]);
                             if (m < p.M && n < p.N)
-                                p.dots[((size_t)m * p.N + n) * G + gg] = (int32_t)d[nb][e];
+                                p.dots[((size_t)m * p.N + n) * G + gg] = (int32_t)rintf(dg * 4096.0f);
                         }
                 } else {
                     const float sr = bf16lo_to_f32(sp), sr8 = bf16hi_to_f32(sp);
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
-                        acc[nb][0] = fmaf(sr, d[nb][0], acc[nb][0]);
-                        acc[nb][1] = fmaf(sr, d[nb][1], acc[nb][1]);
-                        acc[nb][2] = fmaf(sr8, d[nb][2], acc[nb][2]);
-                        acc[nb][3] = fmaf(sr8, d[nb][3], acc[nb][3]);
+                        acc[nb][0] = fmaf(sr, fmaf(nzr, xs[nb][0][g], d[nb][0]), acc[nb][0]);
+                        acc[nb][1] = fmaf(sr, fmaf(nzr, xs[nb][1][g], d[nb][1]), acc[nb][1]);
+                        acc[nb][2] = fmaf(sr8, fmaf(nzr8, xs[nb][0][g], d[nb][2]), acc[nb][2]);
+                        acc[nb][3] = fmaf(sr8, fmaf(nzr8, xs[nb][1][g], d[nb][3]), acc[nb][3]);
                     }
                 }
             }
@@ -175,27 +247,18 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, in
     }
 }
 
-// The dequantized weight is folded into bf16 for W4A16 at M > 16 (NB >= 4).
-template <int NB, W4Mode MODE>
-__host__ __device__ constexpr bool fold_for()
-{
-    return MODE == W4Mode::A16 && NB >= 4;
-}
-
 template <int NB, W4Mode MODE>
 __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Params p)
 {
     constexpr bool FOLD = fold_for<NB, MODE>();
-    constexpr bool A8 = MODE != W4Mode::A16;
     constexpr bool DOTS = MODE == W4Mode::A8_DOTS;
-    constexpr int STAGES = stages_for<NB>();
-    constexpr int WST = WARPS * TILE_BYTES;
-    constexpr int XST = NB * 8 * XROW;
+    constexpr int STAGES = stages_for<NB, MODE>();
+    constexpr int SB = stage_bytes<NB, MODE>();
+    constexpr int XOFF = WARPS * TILE_BYTES;     // activation rows within a stage
+    constexpr int SOFF = XOFF + NB * 8 * XROW;   // group sums within a stage
 
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *sw = smem;
-    uint8_t *sxb = smem + STAGES * WST;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sxb + STAGES * XST);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * SB);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + STAGES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -212,51 +275,61 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     }
     {   // activation rows m >= M of every stage stay zero (never copied into)
         const int pad_rows = NB * 8 - p.M;
-        const int per_stage = pad_rows * (XROW / 16);
-        for (int i = threadIdx.x; i < STAGES * per_stage; i += THREADS) {
-            const int s = i / per_stage, rem = i % per_stage;
-            const int row = p.M + rem / (XROW / 16), col = rem % (XROW / 16);
-            *reinterpret_cast<uint4 *>(sxb + s * XST + row * XROW + col * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        const int xper = pad_rows * (XROW / 16), sper = FOLD ? 0 : pad_rows * (SROW / 16);
+        for (int i = threadIdx.x; i < STAGES * (xper + sper); i += THREADS) {
+            const int s = i / (xper + sper), rem = i % (xper + sper);
+            uint8_t *dst = rem < xper
+                               ? smem + s * SB + XOFF + (p.M + rem / (XROW / 16)) * XROW +
+                                     (rem % (XROW / 16)) * 16
+                               : smem + s * SB + SOFF + (p.M + (rem - xper) / 2) * SROW +
+                                     ((rem - xper) % 2) * 16;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     __syncthreads();
 
+    // stage i processes unit u0 + i = (g, b); both sides step (g, b) along
+    const int g_first = (int)(u0 / p.KB), b_first = (int)(u0 % p.KB);
     int issued = 0;
     if (warp == WARPS) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            auto tiles_of = [&](int i) {
-                const int g = (int)((u0 + i) / p.KB);
-                const int nt = p.T - g * WARPS;
-                return nt < WARPS ? nt : WARPS;
-            };
-            auto issue_w = [&](int i) {
-                const long long u = u0 + i;
-                const int g = (int)(u / p.KB), b = (int)(u % p.KB);
-                const int slot = i % STAGES, nt = tiles_of(i);
-                const uint32_t bar = full0 + 8 * slot;
-                mbar_arrive_expect_tx(bar, (uint32_t)(nt * TILE_BYTES + p.M * 512));
-                for (int w = 0; w < nt; ++w)
-                    bulk_g2s(smem_addr(sw + slot * WST + w * TILE_BYTES),
-                             p.packed + ((size_t)(g * WARPS + w) * p.KB + b) * TILE_BYTES,
-                             TILE_BYTES, bar, pol_w);
-            };
-            auto issue_x = [&](int i) {
-                const int b = (int)((u0 + i) % p.KB);
+            const uint32_t xbytes = (uint32_t)p.M * XROW, sbytes = (uint32_t)p.M * SROW;
+            const uint32_t act_bytes = xbytes + (FOLD ? 0u : sbytes);
+            auto issue_w = [&](int i, int g, int b) {
                 const int slot = i % STAGES;
                 const uint32_t bar = full0 + 8 * slot;
-                for (int m = 0; m < p.M; ++m)
-                    bulk_g2s(smem_addr(sxb + slot * XST + m * XROW),
-                             p.x + (size_t)m * p.K + (size_t)b * 256, 512, bar, pol_x);
+                mbar_arrive_expect_tx(bar, (uint32_t)(WARPS * TILE_BYTES) + act_bytes);
+                bulk_g2s(smem_addr(smem + slot * SB),
+                         p.packed + ((size_t)g * p.KB + b) * (WARPS * TILE_BYTES),
+                         WARPS * TILE_BYTES, bar, pol_w);
+            };
+            auto issue_x = [&](int i, int b) {
+                const int slot = i % STAGES;
+                const uint32_t bar = full0 + 8 * slot;
+                bulk_g2s(smem_addr(smem + slot * SB + XOFF),
+                         p.x + (size_t)b * p.M * (XROW / 2), xbytes, bar, pol_x);
+                if (!FOLD)
+                    bulk_g2s(smem_addr(smem + slot * SB + SOFF),
+                             p.xsum + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
             };
             const int pro = n_iter < STAGES ? n_iter : STAGES;
-            for (int i = 0; i < pro; ++i)
-                issue_w(i);
-            pdl_wait();  // activations may come from the kernel launched just before
-            for (int i = 0; i < pro; ++i)
-                issue_x(i);
+            int g = g_first, b = b_first;
+            for (int i = 0; i < pro; ++i) {
+                issue_w(i, g, b);
+                if (++b == p.KB) {
+                    b = 0;
+                    ++g;
+                }
+            }
+            pdl_wait();  // the activations come from act_prep, launched just before
+            int xb = b_first;
+            for (int i = 0; i < pro; ++i) {
+                issue_x(i, xb);
+                if (++xb == p.KB)
+                    xb = 0;
+            }
             issued = pro;
             for (int i = pro; i < n_iter; ++i) {
                 const int slot = i % STAGES;
@@ -265,21 +338,25 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
                 }
-                issue_w(i);
-                issue_x(i);
+                issue_w(i, g, b);
+                issue_x(i, b);
                 issued = i + 1;
+                if (++b == p.KB) {
+                    b = 0;
+                    ++g;
+                }
             }
         }
     } else {
         // ------------------------------------------------------ consumers
-        pdl_wait();
+        pdl_wait();  // act_prep's outputs (scales, counters) are read below
         float acc[NB][4];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
             acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-        const int g_first = (int)(u0 / p.KB);
         int cur_g = g_first;
         bool ok = true;
+        const int r = lane >> 2, c2 = 2 * (lane & 3);
 
         auto flush = [&](int g) {
             if (DOTS)
@@ -288,31 +365,59 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             if (tile >= p.T)
                 return;
             const long long gb = (long long)g * p.KB, ge = gb + p.KB;
-            const bool complete = gb >= u0 && ge <= u1;
+            if (gb >= u0 && ge <= u1) {  // the whole group is ours: write the outputs
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = nb * 8 + c2 + (e & 1);
+                        const int n = tile * 16 + r + 8 * (e >> 1);
+                        if (m < p.M && n < p.N)
+                            p.out[(size_t)m * p.N + n] =
+                                __float2bfloat16_rn(acc[nb][e] * p.oscale[m]);
+                    }
+                return;
+            }
+            // shared group: publish this warp's partial, count it, and let the
+            // last of the group's contributors sum all partials in CTA order
+            const size_t seg = (size_t)p.M * GROUP_ROWS;
             const int slot = (g == g_first) ? 0 : 1;
-            const int r = lane >> 2, c2 = 2 * (lane & 3);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int row = r + 8 * (e >> 1);
                     const int m = nb * 8 + c2 + (e & 1);
-                    const int n = tile * 16 + row;
-                    if (m < p.M && n < p.N) {
-                        if (complete) {
-                            const float v = A8 ? acc[nb][e] * p.sx[m] : acc[nb][e];
-                            p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
-                        } else {
-                            p.partial[((size_t)(c * 2 + slot) * p.M + m) * 128 + warp * 16 + row] =
-                                acc[nb][e];
-                        }
-                    }
+                    const int row = r + 8 * (e >> 1);
+                    if (m < p.M)
+                        p.partial[(size_t)(c * 2 + slot) * seg + (size_t)m * GROUP_ROWS +
+                                  warp * 16 + row] = acc[nb][e];
                 }
+            const int cf = range_owner(p, gb), cl = range_owner(p, ge - 1);
+            unsigned last = 0;
+            __threadfence();
+            __syncwarp();
+            if (lane == 0)
+                last = (atomicAdd(&p.counters[(size_t)g * WARPS + warp], 1u) ==
+                        (unsigned)(cl - cf));
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last)
+                return;
+            __threadfence();
+            const int slot0 = (range_begin(p, cf) == gb) ? 0 : 1;
+            for (int i = lane; i < p.M * 16; i += 32) {
+                const int m = i / 16, row = i % 16;
+                const int n = tile * 16 + row;
+                const size_t off = (size_t)m * GROUP_ROWS + warp * 16 + row;
+                float v = __ldcg(p.partial + (size_t)(cf * 2 + slot0) * seg + off);
+                for (int cc = cf + 1; cc <= cl; ++cc)
+                    v += __ldcg(p.partial + (size_t)(cc * 2) * seg + off);
+                if (n < p.N)
+                    p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v * p.oscale[m]);
+            }
         };
 
+        int g = g_first, b = b_first;
         for (int i = 0; i < n_iter; ++i) {
-            const long long u = u0 + i;
-            const int g = (int)(u / p.KB), b = (int)(u % p.KB);
             if (g != cur_g) {
                 flush(cur_g);
 #pragma unroll
@@ -328,17 +433,22 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             }
             const int tile = g * WARPS + warp;
             if (tile < p.T)
-                compute_stage<NB, FOLD, DOTS>(smem_addr(sw + slot * WST + warp * TILE_BYTES),
-                                              smem_addr(sxb + slot * XST), lane, acc, p, tile, b);
+                compute_stage<NB, FOLD, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
+                                              smem_addr(smem + slot * SB + XOFF),
+                                              smem_addr(smem + slot * SB + SOFF), lane, acc, p,
+                                              tile, b);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * slot);
+            if (++b == p.KB) {
+                b = 0;
+                ++g;
+            }
         }
         if (ok && n_iter > 0)
             flush(cur_g);
     }
 
-    pdl_launch_dependents();
     __syncthreads();
     // Drain: every issued stage's copies must have landed before the CTA's
     // shared memory goes away (only the error path can leave some pending).
@@ -353,50 +463,117 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     }
 }
 
-// Sums the partials of every tile group that several CTAs share, in CTA
-// order, and writes its bf16 outputs.
-template <bool A8>
-__global__ void __launch_bounds__(256) w4_fixup_kernel(const Params p)
+// Activation preparation, one CTA per row (see the file comment), plus the
+// zeroing of the split-K counters.  KIND: PREP_A16 (power-of-two prescale
+// and group sums), PREP_COPY (folded W4A16: x copied as is, scale 1),
+// PREP_A8 (the W4A8 quantizer).  Outputs are super-block-major:
+// xp[(k/256)*M + m][264] (16 pad bytes per row) and xsum[(g/8)*M + m][8].
+enum { PREP_A16 = 0, PREP_COPY = 1, PREP_A8 = 2 };
+
+template <int KIND>
+__global__ void __launch_bounds__(512) act_prep_kernel(const __nv_bfloat16 *__restrict__ x, int M,
+                                                       int K, __nv_bfloat16 *__restrict__ xp,
+                                                       float *__restrict__ xsum,
+                                                       float *__restrict__ oscale,
+                                                       unsigned *__restrict__ counters,
+                                                       int ncounters)
 {
-    pdl_wait();
-    const int g = blockIdx.x;
-    const long long gb = (long long)g * p.KB, ge = gb + p.KB;
-    int lo = 0, hi = p.P - 1;  // the CTA holding unit gb: largest c with begin(c) <= gb
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (range_begin(p, mid) <= gb)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const int c_first = lo;
-    if (range_begin(p, c_first + 1) >= ge)
-        return;  // the whole group lies in one CTA's range: written directly
-    for (int i = threadIdx.x; i < p.M * 128; i += blockDim.x) {
-        const int m = i / 128, row = i % 128;
-        const int n = g * 128 + row;
-        if (n >= p.N)
-            continue;
-        float v = 0.f;
-        for (int c = c_first; c < p.P && range_begin(p, c) < ge; ++c) {
-            const int slot = (range_begin(p, c) / p.KB == g) ? 0 : 1;
-            v += p.partial[((size_t)(c * 2 + slot) * p.M + m) * 128 + row];
+    pdl_launch_dependents();  // the main kernel may start streaming weights
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncounters; i += gridDim.x * blockDim.x)
+        counters[i] = 0u;
+    __shared__ float red[16];
+    const int m = blockIdx.x;
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
+    const int n8 = K / 8;
+    float a = 0.f;
+    if (KIND != PREP_COPY) {
+        for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+            const uint4 v = row[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
         }
-        if (A8)
-            v *= p.sx[m];
-        p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if ((threadIdx.x & 31) == 0)
+            red[threadIdx.x >> 5] = a;
+        __syncthreads();
+        a = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+            a = fmaxf(a, red[i]);
+    }
+    float sxm = 0.f;  // W4A8 activation scale
+    int sigma = 0;    // x' = value * 2^sigma on lower half-steps (2^(sigma-4) upper)
+    if (KIND == PREP_A8) {
+        sxm = __fdiv_rn(a, 127.0f);
+        sigma = 121;
+    } else if (KIND == PREP_A16) {
+        int e = 0;
+        if (a > 0.f)
+            (void)frexpf(a, &e);  // a < 2^e
+        sigma = min(max(128 - e, 6), 259);
+    }
+    if (threadIdx.x == 0)
+        oscale[m] = KIND == PREP_A8 ? sxm * 4096.0f
+                                    : (KIND == PREP_A16 ? ldexpf(1.0f, 133 - sigma) : 1.0f);
+    // 8 consecutive values per thread; 4 threads per group of 32
+    for (int i = threadIdx.x; i < ((n8 + 31) & ~31); i += blockDim.x) {
+        float v[8], part = 0.f;
+        const bool live = i < n8;
+        const int k0 = 8 * i;
+        if (live) {
+            const uint4 raw = row[i];
+            uint4 o = raw;
+            if (KIND != PREP_COPY) {
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = bf16lo_to_f32(w[j]);
+                    v[2 * j + 1] = bf16hi_to_f32(w[j]);
+                }
+                if (KIND == PREP_A8) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        v[j] = (a == 0.f) ? 0.f
+                                          : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxm)), -127.f), 127.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    part += v[j];
+                // columns 8i .. 8i+7: upper half of a 16-column step when i is odd
+                const int sh = (i & 1) ? sigma - 4 : sigma;
+                uint32_t ow[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    ow[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j], sh))) |
+                            ((uint32_t)__bfloat16_as_ushort(
+                                 __float2bfloat16_rn(ldexpf(v[2 * j + 1], sh)))
+                             << 16);
+                o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+            const size_t dst = ((size_t)(k0 / 256) * M + m) * 264 + (k0 % 256);
+            *reinterpret_cast<uint4 *>(xp + dst) = o;
+        }
+        if (KIND != PREP_COPY) {
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            if (live && (i & 3) == 0) {
+                const int g = i / 4;
+                xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] =
+                    ldexpf(part, KIND == PREP_A8 ? -12 : sigma - 133);
+            }
+        }
     }
 }
 
-// W4A8 activation quantizer: per row, sx = fp32(max|x| / 127),
-// xq = clamp(rint(fp32(x / sx)), -127, 127), 0 for an all-zero row.
-// OUT_BF16 writes xq as exact bf16 integers (the MMA operand); otherwise int8.
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(512) act_quant_kernel(const __nv_bfloat16 *__restrict__ x,
-                                                        int K, void *__restrict__ xq,
-                                                        float *__restrict__ sx)
+// W4A8 activation quantizer alone (int8 output; the test view of the same
+// rule act_prep applies).
+__global__ void __launch_bounds__(512) act_quant_i8_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                           int K, int8_t *__restrict__ xq,
+                                                           float *__restrict__ sx)
 {
-    pdl_launch_dependents();
     __shared__ float red[16];
     const int m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
@@ -424,34 +601,14 @@ __global__ void __launch_bounds__(512) act_quant_kernel(const __nv_bfloat16 *__r
     for (int i = threadIdx.x; i < n8; i += blockDim.x) {
         const uint4 v = row[i];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float q[8];
+        uint32_t q[2] = {0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            q[2 * j] = bf16lo_to_f32(w[j]);
-            q[2 * j + 1] = bf16hi_to_f32(w[j]);
+        for (int j = 0; j < 8; ++j) {
+            const float f = (j & 1) ? bf16hi_to_f32(w[j / 2]) : bf16lo_to_f32(w[j / 2]);
+            const float qf = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(f, s)), -127.f), 127.f);
+            q[j / 4] |= (uint32_t)(uint8_t)(int8_t)qf << (8 * (j % 4));
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            q[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(q[j], s)), -127.f), 127.f);
-        if (OUT_BF16) {
-            uint4 o;
-            o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[0])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[1])) << 16);
-            o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[2])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[3])) << 16);
-            o.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[4])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[5])) << 16);
-            o.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[6])) |
-                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q[7])) << 16);
-            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(xq) + (size_t)m * K)[i] = o;
-        } else {
-            uint2 o;
-            o.x = (uint32_t)(uint8_t)(int8_t)q[0] | ((uint32_t)(uint8_t)(int8_t)q[1] << 8) |
-                  ((uint32_t)(uint8_t)(int8_t)q[2] << 16) | ((uint32_t)(uint8_t)(int8_t)q[3] << 24);
-            o.y = (uint32_t)(uint8_t)(int8_t)q[4] | ((uint32_t)(uint8_t)(int8_t)q[5] << 8) |
-                  ((uint32_t)(uint8_t)(int8_t)q[6] << 16) | ((uint32_t)(uint8_t)(int8_t)q[7] << 24);
-            reinterpret_cast<uint2 *>(static_cast<int8_t *>(xq) + (size_t)m * K)[i] = o;
-        }
+        reinterpret_cast<uint2 *>(xq + (size_t)m * K)[i] = make_uint2(q[0], q[1]);
     }
 }
 
@@ -465,9 +622,9 @@ int ctas_per_sm(int dev)
         return 1;
     if (cache[dev] == 0) {
         auto fn = w4_kernel<NB, MODE>;
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for<NB>());
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for<NB, MODE>());
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, THREADS, smem_for<NB>()) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, THREADS, smem_for<NB, MODE>()) !=
                 cudaSuccess ||
             n < 1)
             n = 1;
@@ -490,53 +647,62 @@ int ctas_per_sm_for(int NB, int dev)
 }
 
 template <int NB, W4Mode MODE>
-cudaError_t launch_main(const Params &p, cudaStream_t stream, bool pdl)
+cudaError_t launch_main(const Params &p, cudaStream_t stream)
 {
     auto fn = w4_kernel<NB, MODE>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_for<NB>());
+                                         smem_for<NB, MODE>());
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.P);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = smem_for<NB>();
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fn, p);
-}
-
-template <W4Mode MODE>
-cudaError_t dispatch_main(const W4Plan &plan, const Params &p, cudaStream_t stream, bool pdl)
-{
-    switch (plan.NB) {
-    case 1: return launch_main<1, MODE>(p, stream, pdl);
-    case 2: return launch_main<2, MODE>(p, stream, pdl);
-    case 4: return launch_main<4, MODE>(p, stream, pdl);
-    default: return launch_main<8, MODE>(p, stream, pdl);
-    }
-}
-
-template <bool A8>
-cudaError_t launch_fixup(const Params &p, cudaStream_t stream)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.G);
-    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem_for<NB, MODE>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w4_fixup_kernel<A8>, p);
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <W4Mode MODE>
+cudaError_t dispatch_main(const W4Plan &plan, const Params &p, cudaStream_t stream)
+{
+    switch (plan.NB) {
+    case 1: return launch_main<1, MODE>(p, stream);
+    case 2: return launch_main<2, MODE>(p, stream);
+    case 4: return launch_main<4, MODE>(p, stream);
+    default: return launch_main<8, MODE>(p, stream);
+    }
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace layout: [x' bf16 (K/256)*M*264][X' f32 (K/256)*M*8][out scale f32 M]
+//                   [counters u32 G*8][partials f32 P*2*M*128], 256-byte aligned.
+struct WsLayout {
+    size_t xp, xsum, oscale, counters, partial, total;
+};
+
+WsLayout ws_layout(const W4Plan &pl)
+{
+    WsLayout L;
+    size_t o = 0;
+    L.xp = o;
+    o += align_up((size_t)pl.KB * pl.M * XROW, 256);
+    L.xsum = o;
+    o += pl.fold ? 0 : align_up((size_t)pl.KB * pl.M * SROW, 256);
+    L.oscale = o;
+    o += align_up((size_t)pl.M * 4, 256);
+    L.counters = o;
+    o += pl.fixup ? align_up((size_t)pl.G * WARPS * 4, 256) : 0;
+    L.partial = o;
+    o += pl.partial_bytes;
+    L.total = o;
+    return L;
+}
 
 }  // namespace
 
@@ -576,23 +742,23 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     }
     if (mode == W4Mode::A8_DOTS)
         pl.fixup = false;
-    pl.partial_bytes = pl.fixup ? (size_t)pl.P * 2 * M * 128 * sizeof(float) : 0;
+    pl.partial_bytes = pl.fixup ? (size_t)pl.P * 2 * M * GROUP_ROWS * sizeof(float) : 0;
     *plan = pl;
     return true;
 }
 
 size_t w4_workspace_for(const W4Plan &plan, W4Mode mode)
 {
-    size_t bytes = plan.partial_bytes;
-    if (mode != W4Mode::A16)
-        bytes += align_up((size_t)plan.M * plan.K * 2, 256) + align_up((size_t)plan.M * 4, 256);
-    return bytes;
+    (void)mode;
+    return ws_layout(plan).total;
 }
 
 cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void *packed,
                       void *out, int32_t *dots, void *workspace, unsigned *err,
                       cudaStream_t stream)
 {
+    const WsLayout L = ws_layout(plan);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
     Params p = {};
     p.packed = static_cast<const uint8_t *>(packed);
     p.out = static_cast<__nv_bfloat16 *>(out);
@@ -607,40 +773,40 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     p.P = plan.P;
     p.split = plan.split;
     p.U = (long long)plan.G * plan.KB;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    cudaError_t e;
-    if (mode == W4Mode::A16) {
-        p.x = static_cast<const __nv_bfloat16 *>(x);
-        p.partial = reinterpret_cast<float *>(ws);
-        e = dispatch_main<W4Mode::A16>(plan, p, stream, false);
-        if (e == cudaSuccess && plan.fixup)
-            e = launch_fixup<false>(p, stream);
-        return e;
-    }
-    __nv_bfloat16 *xq = reinterpret_cast<__nv_bfloat16 *>(ws);
-    float *sx = reinterpret_cast<float *>(ws + align_up((size_t)plan.M * plan.K * 2, 256));
-    p.x = xq;
-    p.sx = sx;
-    p.partial = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(sx) +
-                                          align_up((size_t)plan.M * 4, 256));
-    act_quant_kernel<true><<<plan.M, 512, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                       plan.K, xq, sx);
-    e = cudaGetLastError();
+    p.x = reinterpret_cast<const __nv_bfloat16 *>(ws + L.xp);
+    p.xsum = reinterpret_cast<const float *>(ws + L.xsum);
+    p.oscale = reinterpret_cast<const float *>(ws + L.oscale);
+    p.counters = reinterpret_cast<unsigned *>(ws + L.counters);
+    p.partial = reinterpret_cast<float *>(ws + L.partial);
+    const int ncounters = plan.fixup ? plan.G * WARPS : 0;
+    __nv_bfloat16 *xp = reinterpret_cast<__nv_bfloat16 *>(ws + L.xp);
+    float *xsum = reinterpret_cast<float *>(ws + L.xsum);
+    float *osc = reinterpret_cast<float *>(ws + L.oscale);
+    unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.counters);
+    const __nv_bfloat16 *xin = static_cast<const __nv_bfloat16 *>(x);
+    if (mode == W4Mode::A16 && plan.fold)
+        act_prep_kernel<PREP_COPY><<<plan.M, 512, 0, stream>>>(xin, plan.M, plan.K, xp, xsum, osc,
+                                                               cnt, ncounters);
+    else if (mode == W4Mode::A16)
+        act_prep_kernel<PREP_A16><<<plan.M, 512, 0, stream>>>(xin, plan.M, plan.K, xp, xsum, osc,
+                                                              cnt, ncounters);
+    else
+        act_prep_kernel<PREP_A8><<<plan.M, 512, 0, stream>>>(xin, plan.M, plan.K, xp, xsum, osc,
+                                                             cnt, ncounters);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    if (mode == W4Mode::A8_DOTS)
-        return dispatch_main<W4Mode::A8_DOTS>(plan, p, stream, true);
-    e = dispatch_main<W4Mode::A8>(plan, p, stream, true);
-    if (e == cudaSuccess && plan.fixup)
-        e = launch_fixup<true>(p, stream);
-    return e;
+    if (mode == W4Mode::A16)
+        return dispatch_main<W4Mode::A16>(plan, p, stream);
+    if (mode == W4Mode::A8)
+        return dispatch_main<W4Mode::A8>(plan, p, stream);
+    return dispatch_main<W4Mode::A8_DOTS>(plan, p, stream);
 }
 
 cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *sx,
                                 cudaStream_t stream)
 {
-    act_quant_kernel<false><<<M, 512, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), K, xq,
-                                                   sx);
+    act_quant_i8_kernel<<<M, 512, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), K, xq, sx);
     return cudaGetLastError();
 }
 

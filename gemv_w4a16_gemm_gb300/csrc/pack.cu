@@ -11,9 +11,16 @@ namespace {
 
 constexpr int TILE_BYTES = 2432;
 
-// One CTA quantizes one 16-row x 256-K tile: thread (rr, gg) owns row rr and
-// group gg (8 groups of 32), then the CTA writes the tile's 2432 bytes with
-// coalesced 32-bit stores.
+// Tiles are ordered (128-row group, super-block, row tile of the group).
+__host__ __device__ __forceinline__ size_t tile_offset(int t, int b, int KB)
+{
+    return (((size_t)(t / 8) * KB + b) * 8 + t % 8) * TILE_BYTES;
+}
+
+// One CTA quantizes one 16-row x 256-K tile (every tile of the padded
+// layout, all-zero rows included): thread (rr, gg) owns row rr and group gg
+// (8 groups of 32), then the CTA writes the tile's 2432 bytes with coalesced
+// 32-bit stores.
 __global__ void __launch_bounds__(128) pack_kernel(const __nv_bfloat16 *__restrict__ W,
                                                    uint8_t *__restrict__ packed, int N, int K)
 {
@@ -79,20 +86,22 @@ __global__ void __launch_bounds__(128) pack_kernel(const __nv_bfloat16 *__restri
     }
     __syncthreads();
 
-    uint32_t *tile = reinterpret_cast<uint32_t *>(packed + ((size_t)t * KB + b) * TILE_BYTES);
+    uint32_t *tile = reinterpret_cast<uint32_t *>(packed + tile_offset(t, b, KB));
     // nibble words: word index 128*sb + 4*l + j
     for (int wi = threadIdx.x; wi < 512; wi += 128) {
         const int sb = wi / 128, l = (wi / 4) % 32, j = wi % 4;
         const int r = l / 4, c = 2 * (l % 4);
         uint32_t word = 0;
 #pragma unroll
-        for (int p = 0; p < 4; ++p)
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = r + 8 * (p & 1);
-                const int col = 64 * sb + 16 * j + c + 8 * (p >> 1) + h;
-                word |= (uint32_t)codes[row][col] << (4 * p + 16 * h);
-            }
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = r + 8 * a;
+                    const int col = 64 * sb + 16 * j + c + 8 * e + h;
+                    word |= (uint32_t)codes[row][col] << (8 * a + 4 * e + 16 * h);
+                }
         tile[wi] = word;
     }
     // scale words: word 32*(g/4) + 4*r + g%4 holds (s[r][g], s[r+8][g])
@@ -124,13 +133,13 @@ __global__ void unpack_kernel(const uint8_t *__restrict__ packed, uint8_t *__res
         const int sb = kk / 64, j = (kk % 64) / 16, col = kk % 16;
         const int r = rr % 8, prow = rr / 8, chi = col / 8, cc = col % 8;
         const int h = cc % 2, c = cc - h;
-        const int l = 4 * r + c / 2, p = prow + 2 * chi;
-        const int bit = 4 * p + 16 * h;
-        const size_t byte = ((size_t)t * KB + b) * TILE_BYTES + 512 * sb + 16 * l + 4 * j + bit / 8;
+        const int l = 4 * r + c / 2;
+        const int bit = 8 * prow + 4 * chi + 16 * h;
+        const size_t byte = tile_offset(t, b, KB) + 512 * sb + 16 * l + 4 * j + bit / 8;
         q[i] = (packed[byte] >> (bit % 8)) & 0xF;
         if (kk % 32 == 0) {
             const int gg = kk / 32;
-            const size_t tile = ((size_t)t * KB + b) * TILE_BYTES;
+            const size_t tile = tile_offset(t, b, KB);
             const size_t sbyte = tile + 2048 + 128 * (gg / 4) + 16 * r + 4 * (gg % 4) + 2 * prow;
             scale[(size_t)n * G + k / 32] =
                 (uint16_t)(packed[sbyte] | ((uint16_t)packed[sbyte + 1] << 8));
@@ -143,7 +152,7 @@ __global__ void unpack_kernel(const uint8_t *__restrict__ packed, uint8_t *__res
 
 cudaError_t launch_pack(const void *W, void *packed, int N, int K, cudaStream_t stream)
 {
-    const int tiles = ((N + 15) / 16) * (K / 256);
+    const int tiles = ((N + 127) / 128) * 8 * (K / 256);
     pack_kernel<<<tiles, 128, 0, stream>>>(static_cast<const __nv_bfloat16 *>(W),
                                            static_cast<uint8_t *>(packed), N, K);
     return cudaGetLastError();

@@ -10,14 +10,17 @@
 // Design (one CTA per SM: 16 consumer warps + 1 producer warp):
 //  * CTA c owns a contiguous range of whole rows; those rows are one
 //    contiguous stretch of W, streamed through a shared-memory ring by 1-D
-//    bulk copies (TMA engine, L2 evict-first), RW rows per stage.
+//    bulk copies (TMA engine, L2 evict-first), RW rows per stage (RW fixed
+//    at compile time: 4 rows for K <= 8192 and M <= 2, else 2 rows).
 //  * Lane (w, l) owns the 16-byte columns k = 16*(256*ch + 32*w + l) + 0..15
 //    of every row; the matching activations sit in its registers as fp32
 //    for the whole kernel, so each weight byte costs one PRMT (it lands in
 //    the mantissa of 2^23 + 128 + b), one FADD and M FMAs.
-//  * Per row, each warp reduces over its lanes with shuffles and parks the
-//    partial in shared memory; the CTA sums the 16 warp partials in a fixed
-//    order, multiplies by the row scale and rounds once to bf16.
+//  * The RW rows of a stage are unrolled, so their FMA chains (two per row
+//    and m) and their warp shuffle reductions are independent and overlap.
+//    Each warp parks its per-row sums in shared memory; the CTA sums the 16
+//    warp partials in a fixed order, multiplies by the row scale and rounds
+//    once to bf16.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,8 +30,8 @@ namespace {
 
 constexpr int CWARPS = 16;                  // consumer warps
 constexpr int THREADS = (CWARPS + 1) * 32;  // + producer warp
-constexpr int STAGES = 6;
-constexpr int STAGE_BYTES = 16384;
+constexpr int STAGES = 5;
+constexpr int STAGE_BYTES = 32768;
 constexpr int MAX_ROWS = 64;                // rows per CTA
 constexpr int LANE_SPAN = CWARPS * 32 * 16; // bytes of a row covered per lane chunk
 
@@ -38,10 +41,10 @@ struct W8Params {
     const __nv_bfloat16 *scales;
     __nv_bfloat16 *out;
     unsigned *err;
-    int N, K, P, RW;
+    int N, K, P;
 };
 
-template <int M, int CH>
+template <int M, int CH, int RW>
 __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
     const int c = blockIdx.x;
     const int r0 = (int)((long long)c * p.N / p.P), r1 = (int)((long long)(c + 1) * p.N / p.P);
     const int rows = r1 - r0;
-    const int n_iter = (rows + p.RW - 1) / p.RW;
+    const int n_iter = (rows + RW - 1) / RW;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -76,8 +79,8 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
                 }
-                const int ra = r0 + i * p.RW;
-                const int nr = (r1 - ra) < p.RW ? (r1 - ra) : p.RW;
+                const int ra = r0 + i * RW;
+                const int nr = (r1 - ra) < RW ? (r1 - ra) : RW;
                 const uint32_t bytes = (uint32_t)nr * (uint32_t)p.K;
                 mbar_arrive_expect_tx(full0 + 8 * slot, bytes);
                 bulk_g2s(smem_addr(ring + slot * STAGE_BYTES), p.W + (size_t)ra * p.K, bytes,
@@ -115,48 +118,56 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
                 report_error(p.err, ERR_FULL_WAIT);
                 break;
             }
-            const int ra = r0 + i * p.RW;
-            const int nr = (r1 - ra) < p.RW ? (r1 - ra) : p.RW;
+            const int ra = r0 + i * RW;
+            const int nr = (r1 - ra) < RW ? (r1 - ra) : RW;
             const uint32_t base = smem_addr(ring + slot * STAGE_BYTES);
-            for (int j = 0; j < nr; ++j) {
-                float acc[M];
+            float acc[RW][M][2];
+#pragma unroll
+            for (int j = 0; j < RW; ++j)
 #pragma unroll
                 for (int m = 0; m < M; ++m)
-                    acc[m] = 0.f;
+                    acc[j][m][0] = acc[j][m][1] = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < CH; ++ch) {
-                    const int k0 = ch * LANE_SPAN + (warp * 32 + lane) * 16;
-                    if (k0 < p.K) {
-                        const uint4 v = lds128(base + (uint32_t)(j * p.K + k0));
-                        const uint32_t wd[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u,
-                                                v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+            for (int j = 0; j < RW; ++j) {
+                if (j < nr) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
+                    for (int ch = 0; ch < CH; ++ch) {
+                        const int k0 = ch * LANE_SPAN + (warp * 32 + lane) * 16;
+                        if (k0 < p.K) {
+                            const uint4 v = lds128(base + (uint32_t)(j * p.K + k0));
+                            const uint32_t wd[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u,
+                                                    v.z ^ 0x80808080u, v.w ^ 0x80808080u};
 #pragma unroll
-                            for (int bt = 0; bt < 4; ++bt) {
-                                // bytes [u, 0, 0, 0x4B]: 2^23 + u, u = b + 128
-                                const float f =
-                                    __uint_as_float(prmt(wd[q], 0x4B000000u, 0x7440u + bt)) -
-                                    8388736.0f;
+                            for (int q = 0; q < 4; ++q)
 #pragma unroll
-                                for (int m = 0; m < M; ++m)
-                                    acc[m] = fmaf(f, xr[ch][4 * q + bt][m], acc[m]);
-                            }
+                                for (int bt = 0; bt < 4; ++bt) {
+                                    // bytes [u, 0, 0, 0x4B]: 2^23 + u, u = b + 128
+                                    const float f =
+                                        __uint_as_float(prmt(wd[q], 0x4B000000u, 0x7440u + bt)) -
+                                        8388736.0f;
+#pragma unroll
+                                    for (int m = 0; m < M; ++m)
+                                        acc[j][m][bt & 1] =
+                                            fmaf(f, xr[ch][4 * q + bt][m], acc[j][m][bt & 1]);
+                                }
+                        }
                     }
-                }
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    float v = acc[m];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0)
-                        red[(warp * MAX_ROWS + (ra - r0 + j)) * M + m] = v;
                 }
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * slot);
+#pragma unroll
+            for (int j = 0; j < RW; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    float v = acc[j][m][0] + acc[j][m][1];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0 && j < nr)
+                        red[(warp * MAX_ROWS + (ra - r0 + j)) * M + m] = v;
+                }
         }
     }
     __syncthreads();
@@ -179,15 +190,15 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
     }
 }
 
-template <int M, int CH>
+template <int M, int CH, int RW>
 cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
 {
     const int smem = STAGES * STAGE_BYTES + CWARPS * MAX_ROWS * M * 4 + 2 * STAGES * 8;
-    cudaError_t e = cudaFuncSetAttribute(w8_kernel<M, CH>,
+    cudaError_t e = cudaFuncSetAttribute(w8_kernel<M, CH, RW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
-    w8_kernel<M, CH><<<p.P, THREADS, smem, stream>>>(p);
+    w8_kernel<M, CH, RW><<<p.P, THREADS, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -196,7 +207,7 @@ cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
 // Supported: 1 <= M <= 4, K % 16 == 0, K <= 16384, M * ceil(K / 8192) <= 4.
 bool w8_supported(int M, int K)
 {
-    if (M < 1 || M > 4 || K < 16 || K % 16 != 0 || K > STAGE_BYTES)
+    if (M < 1 || M > 4 || K < 16 || K % 16 != 0 || K > STAGE_BYTES / 2)
         return false;
     const int ch = (K + LANE_SPAN - 1) / LANE_SPAN;
     return M * ch <= 4;
@@ -217,16 +228,14 @@ cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *
     if (per_cta > MAX_ROWS)
         per_cta = MAX_ROWS;
     p.P = (N + per_cta - 1) / per_cta;
-    int rw = STAGE_BYTES / K;
-    p.RW = rw < 1 ? 1 : (rw > 8 ? 8 : rw);
-    const int ch = (K + LANE_SPAN - 1) / LANE_SPAN;
+    const int ch = (K + LANE_SPAN - 1) / LANE_SPAN;  // 1: K <= 8192 (4 rows/stage), 2: <= 16384
     switch (M * 4 + ch) {
-    case 1 * 4 + 1: return launch_t<1, 1>(p, stream);
-    case 1 * 4 + 2: return launch_t<1, 2>(p, stream);
-    case 2 * 4 + 1: return launch_t<2, 1>(p, stream);
-    case 2 * 4 + 2: return launch_t<2, 2>(p, stream);
-    case 3 * 4 + 1: return launch_t<3, 1>(p, stream);
-    case 4 * 4 + 1: return launch_t<4, 1>(p, stream);
+    case 1 * 4 + 1: return launch_t<1, 1, 4>(p, stream);
+    case 1 * 4 + 2: return launch_t<1, 2, 2>(p, stream);
+    case 2 * 4 + 1: return launch_t<2, 1, 4>(p, stream);
+    case 2 * 4 + 2: return launch_t<2, 2, 2>(p, stream);
+    case 3 * 4 + 1: return launch_t<3, 1, 2>(p, stream);
+    case 4 * 4 + 1: return launch_t<4, 1, 2>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -40,24 +40,29 @@
  *   - Non-finite inputs give unspecified (but memory-safe) outputs.
  *
  * Packed W4 layout (this library's own; the pages' storage is prior art):
- *   Rows are grouped in tiles of 16 (N is padded up to a multiple of 16 with
- *   all-zero rows), K in super-blocks of 256 (8 groups).  Tile (t, b),
- *   t < ceil(N/16), b < K/256, is 2432 bytes at offset (t*(K/256) + b)*2432:
+ *   Rows are grouped in tiles of 16 and tiles in groups of 8 (128 rows; N
+ *   is padded up to a multiple of 128 with all-zero rows), K in super-blocks
+ *   of 256 (8 groups).  Tile (t, b), t < 8*ceil(N/128), b < K/256, is 2432
+ *   bytes at offset (((t/8)*(K/256) + b)*8 + t%8)*2432, so the 8 tiles of a
+ *   (128-row group, super-block) pair are one contiguous 19456-byte block:
  *     [0, 2048)     4-bit codes q.  Sub-block sb = kk/64 (kk = k - 256b) at
  *                   512*sb; "lane" l in 0..31 at +16*l; little-endian 32-bit
  *                   word j = (kk%64)/16 at +4*j.  Inside word j, with
- *                   r = l/4 and c = 2*(l%4), the nibble at bit 4p + 16h
- *                   (p in 0..3, h in 0..1) is the code of row
- *                   16t + r + 8*(p&1) and column 256b + 64sb + 16j + c +
- *                   8*(p>>1) + h.  (One 16-byte lane chunk is exactly the
- *                   four bf16 A fragments of an m16n8k16 MMA for that lane.)
+ *                   r = l/4 and c = 2*(l%4), the nibble at bit 8a + 4e + 16h
+ *                   (a, e, h in 0..1) is the code of row 16t + r + 8a and
+ *                   column 256b + 64sb + 16j + c + 8e + h.  (One 16-byte
+ *                   lane chunk holds the four bf16 A fragments of four
+ *                   m16n8k16 MMAs for that lane; masking a word with
+ *                   0x000F000F / 0x00F000F0, before and after a shift by 8,
+ *                   yields them as exact multiples of a power of two.)
  *     [2048, 2304)  bf16 scales s.  The pair (s[16t+r][8b+g],
  *                   s[16t+r+8][8b+g]) is at 2048 + 128*(g/4) + 16*r +
  *                   4*(g%4), row r first (r in 0..7, g in 0..7).
  *     [2304, 2432)  u8 zero points z, the pair (z[16t+r][8b+g],
  *                   z[16t+r+8][8b+g]) at 2304 + 16*r + 2*g.
- *   Every field starts on a 16-byte boundary, so each CTA streams whole
- *   tiles with 1-D bulk copies and each lane reads 16-byte chunks.
+ *   Every field starts on a 16-byte boundary, so a CTA streams a whole
+ *   128 x 256 block with one 1-D bulk copy and each lane reads 16-byte
+ *   chunks.
  *
  * Quantizer (w4_pack_weights), per row n and group g of 32 columns, with
  * max/min over the group:
@@ -93,8 +98,8 @@ const char *w4q_status_string(int status);
 
 /* ---------------------------------------------------------------- W4 --- */
 
-/* Bytes of the packed W4 buffer for an [N,K] weight: ceil(N/16)*(K/256)*2432.
- * Returns 0 when (N, K, group) is unsupported. */
+/* Bytes of the packed W4 buffer for an [N,K] weight:
+ * ceil(N/128)*8*(K/256)*2432.  Returns 0 when (N, K, group) is unsupported. */
 size_t w4_packed_bytes(int64_t N, int64_t K, int group);
 
 /* Quantize a bf16 weight and write it in the packed layout above.
@@ -129,10 +134,9 @@ size_t w4_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int group,
 int w4_split_choice(int64_t M, int64_t N, int64_t K, int group);
 
 /* Number of kernels one w4a16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1) call
- * with these sizes launches on the current device with the library's own
- * split choice: the main kernel, plus the W4A8 activation quantizer, plus
- * the split-K fixup when a tile group is shared by several CTAs.  -1 when
- * the sizes are unsupported. */
+ * with these sizes launches on the current device: the activation
+ * preparation (W4A8 quantizer / W4A16 power-of-two prescale, split-K
+ * counter reset) and the main kernel.  -1 when the sizes are unsupported. */
 int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
 
 /* out = x . dequant(packed)^T, W4A16.

@@ -49,6 +49,7 @@
 #define TILE_ROWS 16      /* packed layout: rows per tile                */
 #define TILE_K 256        /* packed layout: K per tile (8 groups)        */
 #define TILE_BYTES 2432   /* 2048 nibble bytes + 256 scale + 128 zero    */
+#define GROUP_TILES 8     /* packed layout: row tiles per 128-row group  */
 
 /* ------------------------------------------------------------------ */
 /* bf16 helpers                                                        */
@@ -169,29 +170,40 @@ int64_t oracle_packed_bytes(int64_t N, int64_t K)
 {
     if (N < 1 || K < TILE_K || K % TILE_K != 0)
         return 0;
-    return ((N + TILE_ROWS - 1) / TILE_ROWS) * (K / TILE_K) * TILE_BYTES;
+    int64_t groups = (N + TILE_ROWS * GROUP_TILES - 1) / (TILE_ROWS * GROUP_TILES);
+    return groups * GROUP_TILES * (K / TILE_K) * TILE_BYTES;
+}
+
+/* Byte offset of tile (row tile t, super-block b): tiles are ordered by
+ * 128-row group, then super-block, then the group's 8 row tiles, so the 8
+ * tiles of one (group, super-block) are contiguous. */
+static int64_t tile_offset(int64_t t, int64_t b, int64_t KB)
+{
+    int64_t g = t / GROUP_TILES, w = t % GROUP_TILES;
+    return ((g * KB + b) * GROUP_TILES + w) * TILE_BYTES;
 }
 
 /* Byte offset of the nibble holding q[n][k] inside the packed buffer and
  * the bit shift (0 or 4) inside that byte.  Layout of one tile (16 rows
- * n = 16t + 0..15, 256 K k = 256b + 0..255, at byte (t*KB + b)*2432):
+ * n = 16t + 0..15, 256 K k = 256b + 0..255,
+ * at tile_offset(t, b)):
  *   nibble region: sub-block sb = kk/64 at 512*sb; lane l at 16*l;
  *   little-endian 32-bit word j = (kk%64)/16 at 4*j; inside the word the
- *   nibble of element (row r + 8*(p&1), col c + 8*(p>>1) + h) of the
- *   16x16 block sits at bit 4p + 16h, with r = l/4 and c = 2*(l%4). */
+ *   nibble of element (row r + 8*a, col c + 8*e + h) of the 16x16 block
+ *   sits at bit 8a + 4e + 16h (a, e, h in {0,1}), with r = l/4 and
+ *   c = 2*(l%4). */
 static void nibble_position(int64_t n, int64_t k, int64_t KB, int64_t *byte,
                             int *shift)
 {
     int64_t t = n / TILE_ROWS, b = k / TILE_K;
     int rr = (int)(n % TILE_ROWS), kk = (int)(k % TILE_K);
     int sb = kk / 64, j = (kk % 64) / 16, col = kk % 16;
-    int rlo = rr % 8, p_row = rr / 8;    /* row = r + 8*(p&1)            */
-    int chi = col / 8, cc = col % 8;     /* col = c + 8*(p>>1) + h       */
+    int rlo = rr % 8, a = rr / 8;        /* row = r + 8a                 */
+    int e = col / 8, cc = col % 8;       /* col = c + 8e + h             */
     int h = cc % 2, c = cc - h;          /* c = 2*(l%4)                  */
     int l = rlo * 4 + c / 2;
-    int p = p_row + 2 * chi;
-    int bit = 4 * p + 16 * h;
-    int64_t tile = (t * KB + b) * TILE_BYTES;
+    int bit = 8 * a + 4 * e + 16 * h;
+    int64_t tile = tile_offset(t, b, KB);
     *byte = tile + 512 * sb + 16 * l + 4 * j + bit / 8;
     *shift = bit % 8;
 }
@@ -203,12 +215,13 @@ static void meta_position(int64_t n, int64_t g, int64_t KB, int64_t *sbyte,
     int64_t t = n / TILE_ROWS, b = g / (TILE_K / GROUP);
     int rr = (int)(n % TILE_ROWS), gg = (int)(g % (TILE_K / GROUP));
     int r = rr % 8, half = rr / 8;
-    int64_t tile = (t * KB + b) * TILE_BYTES;
+    int64_t tile = tile_offset(t, b, KB);
     *sbyte = tile + 2048 + 128 * (gg / 4) + 16 * r + 4 * (gg % 4) + 2 * half;
     *zbyte = tile + 2304 + 16 * r + 2 * gg + half;
 }
 
-/* Write q/s/z into the packed layout.  Rows N..ceil(N/16)*16-1 are zero. */
+/* Write q/s/z into the packed layout.  Padding rows (N up to a multiple of
+ * 128) are zero. */
 void oracle_pack_w4(const uint8_t *q, const uint16_t *s, const uint8_t *z,
                     int64_t N, int64_t K, uint8_t *packed)
 {

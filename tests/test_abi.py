@@ -41,7 +41,7 @@ def test_status_strings():
 
 def test_packed_bytes():
     assert w4q.packed_bytes(256, 768) == 116736
-    assert w4q.packed_bytes(257, 256) == 17 * 2432
+    assert w4q.packed_bytes(257, 256) == 3 * 8 * 2432
     assert w4q.packed_bytes(39936, 6656) == 157827072
     assert w4q.packed_bytes(64, 288) == 0          # K % 256 != 0
     assert w4q.packed_bytes(64, 256, 64) == 0      # group != 32

@@ -189,23 +189,26 @@ def test_dequant_is_q_minus_z_times_s():
 def decode_layout(packed, N, K):
     """Second, vectorised reading of the documented layout (independent of
     the oracle's scalar code): returns q [N,K], s [N,K/32], z [N,K/32]."""
-    KB, T = K // 256, (N + 15) // 16
-    tiles = packed.reshape(T, KB, 2432)
+    KB, G = K // 256, (N + 127) // 128
+    T = 8 * G
+    # tiles are ordered (128-row group, super-block, row tile in the group)
+    tiles = packed.reshape(G, KB, 8, 2432).transpose(0, 2, 1, 3).reshape(T, KB, 2432)
     nib = tiles[:, :, :2048].reshape(T, KB, 4, 32, 4, 4)          # sb, lane, word, byte
     words = nib.astype(np.uint32)
     words = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)
     q = np.zeros((T * 16, K), np.uint8)
     for lane in range(32):
         r, c = lane // 4, 2 * (lane % 4)
-        for p in range(4):
-            for h in range(2):
-                row = r + 8 * (p & 1)
-                col = c + 8 * (p >> 1) + h
-                vals = (words[:, :, :, lane, :] >> (4 * p + 16 * h)) & 0xF   # T, KB, sb, word
-                for sb in range(4):
-                    for j in range(4):
-                        k = np.arange(KB) * 256 + 64 * sb + 16 * j + col
-                        q[np.arange(T)[:, None] * 16 + row, k[None, :]] = vals[:, :, sb, j]
+        for a in range(2):          # row half
+            for e in range(2):      # column half
+                for h in range(2):
+                    row = r + 8 * a
+                    col = c + 8 * e + h
+                    vals = (words[:, :, :, lane, :] >> (8 * a + 4 * e + 16 * h)) & 0xF
+                    for sb in range(4):
+                        for j in range(4):
+                            k = np.arange(KB) * 256 + 64 * sb + 16 * j + col
+                            q[np.arange(T)[:, None] * 16 + row, k[None, :]] = vals[:, :, sb, j]
     sc = tiles[:, :, 2048:2304].reshape(T, KB, 2, 8, 4, 2, 2)       # ghi, r, glo, half, byte
     sc = sc[..., 0].astype(np.uint16) | (sc[..., 1].astype(np.uint16) << 8)
     s = np.zeros((T * 16, K // 32), np.uint16)
@@ -222,7 +225,8 @@ def decode_layout(packed, N, K):
 
 def test_packed_size():
     assert oracle.packed_bytes(256, 768) == 16 * 3 * 2432 == 116736
-    assert oracle.packed_bytes(257, 256) == 17 * 2432
+    assert oracle.packed_bytes(257, 256) == 3 * 8 * 2432      # rows padded to 3 * 128
+    assert oracle.packed_bytes(16, 256) == 8 * 2432
     assert oracle.packed_bytes(39936, 6656) == 157827072
     assert oracle.packed_bytes(64, 288) == 0       # K % 256 != 0 is unsupported
 
@@ -250,9 +254,9 @@ def test_pack_hand_derived_positions():
     cases = {  # (n, k) -> (byte, shift) derived by hand from the layout rule
         (0, 0): (0, 0),      # lane 0, word 0, bit 0
         (0, 1): (2, 0),      # h = 1 -> bit 16
-        (8, 0): (0, 4),      # p = 1 (row + 8) -> bit 4
-        (0, 8): (1, 0),      # p = 2 (col + 8) -> bit 8
-        (8, 9): (3, 4),      # p = 3, h = 1 -> bit 28
+        (8, 0): (1, 0),      # a = 1 (row + 8) -> bit 8
+        (0, 8): (0, 4),      # e = 1 (col + 8) -> bit 4
+        (8, 9): (3, 4),      # a = 1, e = 1, h = 1 -> bit 28
         (1, 0): (64, 0),     # r = 1 -> lane 4
         (0, 2): (16, 0),     # c = 2 -> lane 1
         (0, 16): (4, 0),     # word 1
@@ -266,6 +270,15 @@ def test_pack_hand_derived_positions():
         nz = np.flatnonzero(packed)
         assert list(nz) == [byte], (n, k)
         assert packed[byte] == 0xB << shift, (n, k)
+    # tile order: (row 16*9 + 3, k 256*2 + 5) sits in group 1, super-block 2,
+    # row tile 1 of the group -> tile index (1*KB + 2)*8 + 1 with KB = 3
+    N2, K2 = 300, 768
+    q2 = np.zeros((N2, K2), np.uint8)
+    q2[16 * 9 + 3, 256 * 2 + 5] = 0x7
+    packed2 = oracle.pack_w4(q2, np.zeros((N2, K2 // 32), np.uint16), np.zeros((N2, K2 // 32), np.uint8))
+    tile = ((1 * 3 + 2) * 8 + 1) * 2432
+    # r = 3, c = 4 (col 5 = c + h with h = 1) -> lane 14, word 0, bit 16
+    assert list(np.flatnonzero(packed2)) == [tile + 16 * 14 + 2]
     # scale of (row 9, group 5): r = 1, half = 1 -> 2048 + 128 + 16 + 4 + 2
     s = np.zeros((N, 8), np.uint16)
     s[9, 5] = 0x1234
