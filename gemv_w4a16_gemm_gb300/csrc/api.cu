@@ -123,6 +123,12 @@ size_t workspace_common(int64_t M, int64_t N, int64_t K, int group, int split)
 
 }  // namespace
 
+namespace w4q {
+// Internal accessors for other translation units of the library.
+int device_sm_count(int dev) { return sm_count(dev); }
+unsigned *device_error_word(int dev) { return error_word(dev); }
+}  // namespace w4q
+
 extern "C" {
 
 const char *w4q_status_string(int status)

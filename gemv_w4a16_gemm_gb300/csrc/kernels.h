@@ -46,6 +46,10 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
 cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *sx,
                                 cudaStream_t stream);
 
+// --- per-device state kept by api.cu
+int device_sm_count(int dev);
+unsigned *device_error_word(int dev);  // nullptr if the symbol lookup failed
+
 // --- W8 GEMV (w8.cu)
 cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *out, int M, int N,
                       int K, int sm_count, unsigned *err, cudaStream_t stream);

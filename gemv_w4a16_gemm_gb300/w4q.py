@@ -40,6 +40,7 @@ SIGNATURES = {
     "w4_kernel_launches": (_INT, [_I64, _I64, _I64, _INT, _INT]),
     "w4a16_gemm": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _P, _SZ, _P]),
     "w4a16_gemm_split": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _SZ, _P]),
+    "w4a16_gemm_noalloc": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _P]),
     "w4a8_gemm": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _P, _SZ, _P]),
     "w4a8_gemm_split": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _SZ, _P]),
     "w4a8_quantize_act": (_INT, [_P, _I64, _I64, _P, _P, _P]),
@@ -173,6 +174,20 @@ def _gemm(name, x, packed, N, K, group, split_k, out, workspace, stream):
 def w4a16_gemm(x, packed, N, K, group=GROUP, split_k=None, out=None, workspace=None, stream=None):
     """out[M,N] = x . dequant(packed)^T (W4A16); split_k None = library choice."""
     return _gemm("w4a16_gemm", x, packed, N, K, group, split_k, out, workspace, stream)
+
+
+def w4a16_gemm_noalloc(x, packed, N, K, group=GROUP, out=None, stream=None):
+    """W4A16 without any workspace: the library's own static scratch array is
+    used (for callers that cannot allocate; see include/w4q.h)."""
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, %d]" % K)
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _check("w4a16_gemm_noalloc", lib().w4a16_gemm_noalloc(
+        _cuda(x, torch.bfloat16, "x"), _cuda(packed, torch.uint8, "packed"),
+        _cuda(out, torch.bfloat16, "out"), M, N, K, group, _stream(stream)))
+    return out
 
 
 def w4a8_gemm(x, packed, N, K, group=GROUP, split_k=None, out=None, workspace=None, stream=None):

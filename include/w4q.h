@@ -164,6 +164,30 @@ int w4a16_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
                      int64_t M, int64_t N, int64_t K, int group, int split_k,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* W4A16 for callers that cannot allocate device memory at all.  (The pages
+ * have no counterpart; this is a property of this library's interface.)
+ * Some callers may not call cudaMalloc on the path that runs a layer and
+ * have no workspace to give: code running while a stream is captured into
+ * a CUDA graph, hosts that plan all device memory ahead of time (embedded
+ * or real-time loops that must not pause in an allocator), plug-ins whose
+ * device memory belongs to a host framework.  This call computes exactly
+ * what w4a16_gemm computes, with the same kernels, but takes its scratch
+ * from one array of W4Q_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory
+ * that the library itself holds on every GPU that loads it, until exit.
+ *   x, packed, out, M, N, K, group, stream: as w4a16_gemm.
+ * Returns W4Q_ERR_UNSUPPORTED when the call would need more scratch than
+ * the array holds (large M together with a wide split-K partition; see
+ * w4_workspace_bytes for the amount), besides the w4a16_gemm errors.  It
+ * calls no allocator of any kind.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress), so make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * array: calls that may overlap on the GPU (other streams, other host
+ * threads) race and give wrong results; serialize them.  Each call resets
+ * the part of the array that must start at zero itself. */
+#define W4Q_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int w4a16_gemm_noalloc(const void *x_bf16, const void *packed, void *out_bf16, int64_t M,
+                       int64_t N, int64_t K, int group, void *stream);
+
 /* out = x . dequant(packed)^T, W4A8: per row m, sx = fp32(max|x| / 127),
  * xq = clamp(rint(x / sx), -127, 127) in IEEE fp32 (xq = 0 when max|x| = 0);
  * per group D = sum_k (q - z) * xq, an exact integer (|D| <= 60960);
