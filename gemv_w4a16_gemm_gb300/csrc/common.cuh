@@ -93,6 +93,20 @@ __device__ __forceinline__ void report_error(unsigned *err, unsigned code)
     atomicOr(err, code);
 }
 
+// Device-scope atomic add with acquire-release ordering: writes made before
+// it (by this thread, or by the warp through a preceding __syncwarp) are
+// visible to whoever observes the increment, and reads after it see what
+// the other incrementers wrote before theirs.
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned *addr, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(addr), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // ------------------------------------------------------------ bulk copies
 
 // L2 eviction-priority policies for cp.async.bulk's cache hint.

@@ -7,7 +7,7 @@
 // not their code.)
 //
 // Two launches per call:
-//  1. act_prep (one CTA per activation row) prepares the activation operand
+//  1. act_prep (a few CTAs per activation row) prepares the activation operand
 //     in the workspace, super-block-major ([K/256][M][256 + 8 pad] bf16 and
 //     [K/256][M][8] fp32, so one bulk copy moves a stage's rows), and zeroes
 //     the split-K counters:
@@ -314,9 +314,15 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                     bulk_g2s(smem_addr(smem + slot * SB + SOFF),
                              p.xsum + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
             };
+            // Prologue: two stages of weights go out at once; the activation
+            // copies follow as soon as act_prep has finished.  The other
+            // stages wait until stage 0 has landed, so that at kernel start
+            // every CTA's first stage is not queued behind the whole ring of
+            // every other CTA.
             const int pro = n_iter < STAGES ? n_iter : STAGES;
+            const int first = pro < 2 ? pro : 2;
             int g = g_first, b = b_first;
-            for (int i = 0; i < pro; ++i) {
+            for (int i = 0; i < first; ++i) {
                 issue_w(i, g, b);
                 if (++b == p.KB) {
                     b = 0;
@@ -325,8 +331,21 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             }
             pdl_wait();  // the activations come from act_prep, launched just before
             int xb = b_first;
-            for (int i = 0; i < pro; ++i) {
+            for (int i = 0; i < first; ++i) {
                 issue_x(i, xb);
+                if (++xb == p.KB)
+                    xb = 0;
+            }
+            issued = first;
+            if (pro > first && !mbar_wait_bounded(full0, 0u))
+                report_error(p.err, ERR_FULL_WAIT);
+            for (int i = first; i < pro; ++i) {
+                issue_w(i, g, b);
+                issue_x(i, xb);
+                if (++b == p.KB) {
+                    b = 0;
+                    ++g;
+                }
                 if (++xb == p.KB)
                     xb = 0;
             }
@@ -394,23 +413,32 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 }
             const int cf = range_owner(p, gb), cl = range_owner(p, ge - 1);
             unsigned last = 0;
-            __threadfence();
-            __syncwarp();
+            __syncwarp();  // the warp's partial writes are ordered before lane 0's release
             if (lane == 0)
-                last = (atomicAdd(&p.counters[(size_t)g * WARPS + warp], 1u) ==
+                last = (atomic_add_acq_rel(&p.counters[(size_t)g * WARPS + warp], 1u) ==
                         (unsigned)(cl - cf));
             last = __shfl_sync(0xffffffffu, last, 0);
             if (!last)
                 return;
-            __threadfence();
             const int slot0 = (range_begin(p, cf) == gb) ? 0 : 1;
+            const int nc = cl - cf + 1;
             for (int i = lane; i < p.M * 16; i += 32) {
                 const int m = i / 16, row = i % 16;
                 const int n = tile * 16 + row;
                 const size_t off = (size_t)m * GROUP_ROWS + warp * 16 + row;
-                float v = __ldcg(p.partial + (size_t)(cf * 2 + slot0) * seg + off);
-                for (int cc = cf + 1; cc <= cl; ++cc)
-                    v += __ldcg(p.partial + (size_t)(cc * 2) * seg + off);
+                const float *first = p.partial + (size_t)(cf * 2 + slot0) * seg + off;
+                const float *rest = p.partial + (size_t)(cf * 2 + 2) * seg + off;  // slot 0 of cf+1..
+                float v = __ldcg(first);
+                for (int j = 0; j + 1 < nc; j += 8) {  // eight independent loads, then an in-order sum
+                    float t[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        t[q] = (j + q + 1 < nc) ? __ldcg(rest + (size_t)(j + q) * 2 * seg) : 0.f;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (j + q + 1 < nc)
+                            v += t[q];
+                }
                 if (n < p.N)
                     p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v * p.oscale[m]);
             }
@@ -463,31 +491,37 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     }
 }
 
-// Activation preparation, one CTA per row (see the file comment), plus the
-// zeroing of the split-K counters.  KIND: PREP_A16 (power-of-two prescale
+// Activation preparation (see the file comment), plus the zeroing of the
+// split-K counters.  KIND: PREP_A16 (power-of-two prescale
 // and group sums), PREP_COPY (folded W4A16: x copied as is, scale 1),
 // PREP_A8 (the W4A8 quantizer).  Outputs are super-block-major:
 // xp[(k/256)*M + m][264] (16 pad bytes per row) and xsum[(g/8)*M + m][8].
 enum { PREP_A16 = 0, PREP_COPY = 1, PREP_A8 = 2 };
 
+constexpr int PREP_THREADS = 256;
+constexpr int PREP_CHUNK = PREP_THREADS * 8;  // columns one CTA transforms
+
+// grid = (M, ceil(K / PREP_CHUNK)): every CTA finds the max over its whole
+// row (an L2-resident read of at most a few tens of KB) and transforms one
+// chunk of 2048 columns, so the prepass is one short round trip.
 template <int KIND>
-__global__ void __launch_bounds__(512) act_prep_kernel(const __nv_bfloat16 *__restrict__ x, int M,
-                                                       int K, __nv_bfloat16 *__restrict__ xp,
-                                                       float *__restrict__ xsum,
-                                                       float *__restrict__ oscale,
-                                                       unsigned *__restrict__ counters,
-                                                       int ncounters)
+__global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
+    const __nv_bfloat16 *__restrict__ x, int M, int K, __nv_bfloat16 *__restrict__ xp,
+    float *__restrict__ xsum, float *__restrict__ oscale, unsigned *__restrict__ counters,
+    int ncounters)
 {
     pdl_launch_dependents();  // the main kernel may start streaming weights
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncounters; i += gridDim.x * blockDim.x)
+    const int nblk = gridDim.x * gridDim.y;
+    const int bid = blockIdx.y * gridDim.x + blockIdx.x;
+    for (int i = bid * PREP_THREADS + threadIdx.x; i < ncounters; i += nblk * PREP_THREADS)
         counters[i] = 0u;
-    __shared__ float red[16];
+    __shared__ float red[PREP_THREADS / 32];
     const int m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
     const int n8 = K / 8;
     float a = 0.f;
     if (KIND != PREP_COPY) {
-        for (int i = threadIdx.x; i < n8; i += blockDim.x) {
+        for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
             const uint4 v = row[i];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -501,7 +535,8 @@ __global__ void __launch_bounds__(512) act_prep_kernel(const __nv_bfloat16 *__re
             red[threadIdx.x >> 5] = a;
         __syncthreads();
         a = 0.f;
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+#pragma unroll
+        for (int i = 0; i < PREP_THREADS / 32; ++i)
             a = fmaxf(a, red[i]);
     }
     float sxm = 0.f;  // W4A8 activation scale
@@ -515,55 +550,53 @@ __global__ void __launch_bounds__(512) act_prep_kernel(const __nv_bfloat16 *__re
             (void)frexpf(a, &e);  // a < 2^e
         sigma = min(max(128 - e, 6), 259);
     }
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && blockIdx.y == 0)
         oscale[m] = KIND == PREP_A8 ? sxm * 4096.0f
                                     : (KIND == PREP_A16 ? ldexpf(1.0f, 133 - sigma) : 1.0f);
     // 8 consecutive values per thread; 4 threads per group of 32
-    for (int i = threadIdx.x; i < ((n8 + 31) & ~31); i += blockDim.x) {
-        float v[8], part = 0.f;
-        const bool live = i < n8;
+    const int i = blockIdx.y * PREP_THREADS + threadIdx.x;
+    const bool live = i < n8;
+    float part = 0.f;
+    if (live) {
         const int k0 = 8 * i;
-        if (live) {
-            const uint4 raw = row[i];
-            uint4 o = raw;
-            if (KIND != PREP_COPY) {
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        const uint4 raw = row[i];
+        uint4 o = raw;
+        if (KIND != PREP_COPY) {
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            float v[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v[2 * j] = bf16lo_to_f32(w[j]);
-                    v[2 * j + 1] = bf16hi_to_f32(w[j]);
-                }
-                if (KIND == PREP_A8) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        v[j] = (a == 0.f) ? 0.f
-                                          : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxm)), -127.f), 127.f);
-                }
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = bf16lo_to_f32(w[j]);
+                v[2 * j + 1] = bf16hi_to_f32(w[j]);
+            }
+            if (KIND == PREP_A8) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    part += v[j];
-                // columns 8i .. 8i+7: upper half of a 16-column step when i is odd
-                const int sh = (i & 1) ? sigma - 4 : sigma;
-                uint32_t ow[4];
+                    v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxm)), -127.f), 127.f);
+            }
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    ow[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j], sh))) |
-                            ((uint32_t)__bfloat16_as_ushort(
-                                 __float2bfloat16_rn(ldexpf(v[2 * j + 1], sh)))
-                             << 16);
-                o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-            }
-            const size_t dst = ((size_t)(k0 / 256) * M + m) * 264 + (k0 % 256);
-            *reinterpret_cast<uint4 *>(xp + dst) = o;
+            for (int j = 0; j < 8; ++j)
+                part += v[j];
+            // columns 8i .. 8i+7: upper half of a 16-column step when i is odd
+            const int sh = (i & 1) ? sigma - 4 : sigma;
+            uint32_t ow[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                ow[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j], sh))) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j + 1], sh)))
+                         << 16);
+            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
         }
-        if (KIND != PREP_COPY) {
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            if (live && (i & 3) == 0) {
-                const int g = i / 4;
-                xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] =
-                    ldexpf(part, KIND == PREP_A8 ? -12 : sigma - 133);
-            }
+        const size_t dst = ((size_t)(k0 / 256) * M + m) * 264 + (k0 % 256);
+        *reinterpret_cast<uint4 *>(xp + dst) = o;
+    }
+    if (KIND != PREP_COPY) {
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (live && (i & 3) == 0) {
+            const int g = i / 4;
+            xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] =
+                ldexpf(part, KIND == PREP_A8 ? -12 : sigma - 133);
         }
     }
 }
@@ -784,15 +817,16 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     float *osc = reinterpret_cast<float *>(ws + L.oscale);
     unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.counters);
     const __nv_bfloat16 *xin = static_cast<const __nv_bfloat16 *>(x);
+    const dim3 pgrid((unsigned)plan.M, (unsigned)((plan.K + PREP_CHUNK - 1) / PREP_CHUNK));
     if (mode == W4Mode::A16 && plan.fold)
-        act_prep_kernel<PREP_COPY><<<plan.M, 512, 0, stream>>>(xin, plan.M, plan.K, xp, xsum, osc,
-                                                               cnt, ncounters);
+        act_prep_kernel<PREP_COPY><<<pgrid, PREP_THREADS, 0, stream>>>(xin, plan.M, plan.K, xp,
+                                                                       xsum, osc, cnt, ncounters);
     else if (mode == W4Mode::A16)
-        act_prep_kernel<PREP_A16><<<plan.M, 512, 0, stream>>>(xin, plan.M, plan.K, xp, xsum, osc,
-                                                              cnt, ncounters);
+        act_prep_kernel<PREP_A16><<<pgrid, PREP_THREADS, 0, stream>>>(xin, plan.M, plan.K, xp,
+                                                                      xsum, osc, cnt, ncounters);
     else
-        act_prep_kernel<PREP_A8><<<plan.M, 512, 0, stream>>>(xin, plan.M, plan.K, xp, xsum, osc,
-                                                             cnt, ncounters);
+        act_prep_kernel<PREP_A8><<<pgrid, PREP_THREADS, 0, stream>>>(xin, plan.M, plan.K, xp,
+                                                                     xsum, osc, cnt, ncounters);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
