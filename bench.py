@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import hashlib
 import json
 import os
 import statistics
@@ -38,6 +39,37 @@ import workloads  # noqa: E402
 METRIC = "effective weight GB/s and % of GB300 HBM roofline per call at M=1/4/16/64"
 UNIT = "GB/s"
 WORKLOAD = "decode_linear_suite"
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# the main kernel of a call, from one ncu capture (profiles/ has the command
+# and the counters).  Each figure holds only for the kernel sources it was
+# taken on: the sha256 of those files, concatenated, must still match, else
+# the roofline reports traffic as null.
+MEASURED_TRAFFIC = {
+    "w4a16 N=39936 K=6656 M=64": (
+        164434432, ("gemv_w4.cu", "common.cuh"),
+        "8474da36d5a74f37a8d1966eafac78c2fd2d6035549783d61252dca74fc7e7b5"),
+    "w4a16 N=39936 K=6656 M=4": (
+        161038848, ("gemv_w4.cu", "common.cuh"),
+        "8474da36d5a74f37a8d1966eafac78c2fd2d6035549783d61252dca74fc7e7b5"),
+    "w8 N=8192 K=8192 M=1": (
+        67288576, ("w8.cu", "common.cuh"),
+        "da7b7de323a6abb51a65ed52e37a552be8e2acea241096c0cb5610fca719ef7a"),
+}
+
+
+def measured_traffic(call):
+    """The ncu traffic figure for this call, or None when there is none or
+    the kernel sources changed since it was taken."""
+    entry = MEASURED_TRAFFIC.get(call)
+    if entry is None:
+        return None
+    nbytes, files, digest = entry
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gemv_w4a16_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest() == digest else None
 PAGES_W8_GBS = 1277.19   # "gpt-fast issue #114": compiled int8 GEMV, 8192^2, M=1 (HW unstated)
 
 
@@ -354,7 +386,8 @@ def run_gpu(args, rank, world, dist):
     achieved = dom_alg / dom["us"] / 1e3
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": args.traffic, "kernel": dom["kernel"], "call": dom["call"],
+                "traffic": (args.traffic if args.traffic is not None else measured_traffic(dom["call"])),
+                "kernel": dom["kernel"], "call": dom["call"],
                 "algorithmic_bytes_per_launch": dom_alg, "us_per_launch": round(dom["us"], 3),
                 "peak_source": peaks["source"]}
     value = world * step_weight / (ms * 1e-3) / 1e9
