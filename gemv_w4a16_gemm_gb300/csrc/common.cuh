@@ -88,6 +88,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     }
 }
 
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds in the
+// instruction while the phase is incomplete (it resumes when the phase
+// completes), so a long wait costs no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity), "r"(ns)
+                 : "memory");
+    return ok != 0;
+}
+
+// A wait expected to be long (an epilogue waiting for a whole K range):
+// sleeping polls of at most 20 us each, false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity)
+{
+    const unsigned long long t0 = global_timer();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u))
+        if (global_timer() - t0 > WAIT_LIMIT_NS)
+            return false;
+    return true;
+}
+
 __device__ __forceinline__ void report_error(unsigned *err, unsigned code)
 {
     atomicOr(err, code);

@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 last = (atomic_add_acq_rel(&p.counters[(size_t)g * WARPS + warp], 1u) ==
                         (unsigned)(cl - cf));
             last = __shfl_sync(0xffffffffu, last, 0);
+            __syncwarp();  // lane 0's acquire is ordered before every lane's reads
             if (!last)
                 return;
             const int slot0 = (range_begin(p, cf) == gb) ? 0 : 1;
@@ -752,7 +753,11 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     pl.G = (pl.T + WARPS - 1) / WARPS;
     pl.NB = nb_for(M);
     pl.fold = (mode == W4Mode::A16) && M > 16;
-    const long long U = (long long)pl.G * pl.KB;
+    pl.umma = pl.fold;  // W4A16 above 16 rows runs on the tcgen05 tensor core
+    pl.NP = (M + 15) / 16 * 16;
+    pl.G2 = (pl.G + 1) / 2;
+    const int groups = pl.umma ? pl.G2 : pl.G;  // work-unit rows: tile groups or pairs
+    const long long U = (long long)groups * pl.KB;
     if (mode == W4Mode::A8_DOTS)
         split = 1;  // every unit is processed once; no accumulation across CTAs
     if (split < 0)
@@ -761,13 +766,14 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
         if (split > pl.KB)
             return false;
         pl.split = split;
-        pl.P = pl.G * split;
+        pl.P = groups * split;
         pl.fixup = split > 1;
     } else {
         int dev = 0;
         cudaGetDevice(&dev);
-        const int per_sm = (mode == W4Mode::A16) ? ctas_per_sm_for<W4Mode::A16>(pl.NB, dev)
-                                                 : ctas_per_sm_for<W4Mode::A8>(pl.NB, dev);
+        const int per_sm = pl.umma ? 1
+                           : (mode == W4Mode::A16) ? ctas_per_sm_for<W4Mode::A16>(pl.NB, dev)
+                                                   : ctas_per_sm_for<W4Mode::A8>(pl.NB, dev);
         const long long slots = (long long)(sm_count > 0 ? sm_count : 1) * per_sm;
         pl.split = 0;
         pl.P = (int)(U < slots ? U : slots);
@@ -775,7 +781,9 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     }
     if (mode == W4Mode::A8_DOTS)
         pl.fixup = false;
-    pl.partial_bytes = pl.fixup ? (size_t)pl.P * 2 * M * GROUP_ROWS * sizeof(float) : 0;
+    pl.partial_bytes = !pl.fixup ? 0
+                       : pl.umma ? w4_umma_partial_bytes(pl.P, M)
+                                 : (size_t)pl.P * 2 * M * GROUP_ROWS * sizeof(float);
     *plan = pl;
     return true;
 }
@@ -783,13 +791,15 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
 size_t w4_workspace_for(const W4Plan &plan, W4Mode mode)
 {
     (void)mode;
-    return ws_layout(plan).total;
+    return plan.umma ? w4_umma_workspace(plan) : ws_layout(plan).total;
 }
 
 cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void *packed,
                       void *out, int32_t *dots, void *workspace, unsigned *err,
                       cudaStream_t stream)
 {
+    if (plan.umma)
+        return launch_w4_umma(plan, x, packed, out, workspace, err, stream);
     const WsLayout L = ws_layout(plan);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     Params p = {};

@@ -1,0 +1,634 @@
+// gemv_w4_umma.cu -- W4A16 linear layer for 16 < M <= 64 on the tcgen05
+// tensor core (sm_103a).
+//
+//   out[M,N] = x[M,K] . dequant(Wq)[N,K]^T,   dequant(q) = (q - z) * s
+//
+// ("test_int4_quantized_gemm.py": the dequant + F.linear reference and the
+// W4A16 tile kernels, which dequantize a weight tile to bf16 and run it
+// through the tensor core; this is a new design for GB300, not their code.)
+//
+// At these M the call is a real contraction (2 * M * N * K flops on N*K/2
+// bytes of codes), so the weight is dequantized once and multiplied on the
+// 5th-generation tensor core, with the operands where that core wants them:
+//
+//   * A (weights, 128 rows of a tile group x 16 K per instruction) lives in
+//     tensor memory: dequant warps write (q - z) * s, rounded once to bf16,
+//     straight from registers with 16-lane x 256-bit TMEM stores.  The packed
+//     layout's per-lane words (built for the m16n8k16 fragment) map onto that
+//     store shape one to one, so no shuffles or shared-memory round trip.
+//   * B (activations, M rows padded to NP = 16..64, K-major) lives in shared
+//     memory in the 128-byte-swizzle layout the MMA reads through a matrix
+//     descriptor.  act_prep writes x in exactly that byte order (rows >= M
+//     zero), with the K order inside every 16-column step permuted to match
+//     the column order of the TMEM stores, so one bulk copy per stage lands it.
+//   * D (fp32, 128 lanes x NP columns per tile group) accumulates in tensor
+//     memory over the CTA's whole K range and is read once by the epilogue.
+//
+// One CTA per SM, 15 warps: a producer (bulk copies), two MMA issuers (one
+// thread per tile group of the pair; warp 1 also owns the TMEM allocation),
+// four epilogue warps (one per TMEM lane quarter) and eight dequant warps.  A work unit is a pair of tile
+// groups (256 rows) x one 256-K super-block: both groups share one copy of
+// the activation stage.  Units are split into P contiguous ranges (stream-K,
+// or a fixed split of each pair's K); a pair that one CTA covers entirely is
+// written directly, the others go through fp32 partials, a per-(pair, group,
+// lane quarter) arrival counter, and an in-order sum by the last arriver.
+//
+// Pipelines (every wait bounded by one second of %globaltimer):
+//   producer --full[s]--> dequant + MMA      (packed codes and x of stage s)
+//   dequant  --empty[s]-> producer           (codes read into registers)
+//   MMA      --empty[s]-> producer           (tcgen05.commit: x no longer read)
+//   dequant  --afull[k]-> MMA                (A slot k written to TMEM)
+//   MMA      --aempty[k]-> dequant           (tcgen05.commit: slot k consumed)
+//   MMA      --dfull[d]-> epilogue           (the pair's accumulators final)
+//   epilogue --dempty[d]> MMA                (accumulators read out)
+// The accumulators are double-buffered (d = pair parity), so the MMAs of
+// the next pair do not wait for the epilogue of the last one.
+#include "common.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace w4q {
+
+namespace {
+
+constexpr int UT_TILE_BYTES = 2432;               // 16 rows x 256 K: codes, scales, zeros
+constexpr int UT_GROUP_BYTES = 8 * UT_TILE_BYTES; // one tile group at one super-block
+constexpr int UT_PAIR_ROWS = 256;
+constexpr int UT_EPI_WARPS = 4;
+constexpr int UT_DQ_WARPS = 8;
+constexpr int UT_FIRST_EPI = 2;
+constexpr int UT_FIRST_DQ = UT_FIRST_EPI + UT_EPI_WARPS;
+constexpr int UT_MMA1 = UT_FIRST_DQ + UT_DQ_WARPS;             // MMA issuer of group 1
+constexpr int UT_THREADS = (UT_MMA1 + 1) * 32;                  // 480
+constexpr int UT_NA = 4;             // A slots (one 64-K sub-block of both groups each)
+constexpr uint32_t UT_TMEM_COLS = 512;
+constexpr uint32_t UT_DCOL = 128;    // columns per accumulator buffer (2 groups x NP <= 128)
+constexpr uint32_t UT_ACOL = 256;    // first A column (after two accumulator buffers)
+constexpr int UT_SMEM_LIMIT = 227 * 1024;
+
+struct UParams {
+    const uint8_t *packed;
+    const uint8_t *xs;       // [K/256][4][NP][128 B]: swizzled, K-permuted x (act_prep)
+    __nv_bfloat16 *out;      // bf16 [M][N]
+    float *partial;          // fp32 [P][2][M][256]
+    unsigned *counters;      // [G2][8] arrivals per (pair, group, lane quarter)
+    unsigned *err;
+    int M, N, K, KB, G, G2, P, split;
+    long long U;
+};
+
+template <int NP>
+__host__ __device__ constexpr int ut_stage_bytes()
+{
+    return NP * 512 + 2 * UT_GROUP_BYTES;  // [x: NP x 512][codes of group 0][of group 1]
+}
+
+template <int NP>
+__host__ __device__ constexpr int ut_stages()
+{
+    int s = 4;
+    while (s > 2 && s * ut_stage_bytes<NP>() + 1024 + 512 > UT_SMEM_LIMIT)
+        --s;
+    return s;
+}
+
+template <int NP>
+__host__ __device__ constexpr int ut_smem()
+{
+    return ut_stages<NP>() * ut_stage_bytes<NP>() + 1024;  // + alignment slack
+}
+
+__host__ __device__ __forceinline__ long long ut_range_begin(const UParams &p, int c)
+{
+    if (p.split == 0)
+        return (long long)c * p.U / p.P;
+    const int g = c / p.split, j = c % p.split;
+    return (long long)g * p.KB + (long long)j * p.KB / p.split;
+}
+
+// The CTA whose range holds unit u (the largest c with begin(c) <= u).
+__device__ __forceinline__ int ut_range_owner(const UParams &p, long long u)
+{
+    if (p.split == 0)
+        return (int)(((u + 1) * p.P - 1) / p.U);
+    const int g = (int)(u / p.KB), b = (int)(u % p.KB);
+    return g * p.split + (int)(((long long)(b + 1) * p.split - 1) / p.KB);
+}
+
+// Eight codes of one word -> four bf16x2 A values (q - z) * s of the 16x256b
+// store order: (row r, K pair i), (row r, pair i + 4), (row r + 8, pair i),
+// (row r + 8, pair i + 4), where the word holds rows r, r + 8 and columns
+// 2i, 2i + 1, 2i + 8, 2i + 9 of a 16-column step (nibble of row r + 8a,
+// column 2i + 8e + h at bit 8a + 4e + 16h).
+__device__ __forceinline__ void ut_dequant_word(uint32_t w, uint32_t zr, uint32_t zr8,
+                                                uint32_t s2r, uint32_t s2r8, uint32_t *v)
+{
+    v[0] = bf16x2_mul(bf16x2_sub(and_or(w, 0x000F000Fu, 0x43004300u), zr), s2r);
+    v[1] = bf16x2_mul(bf16x2_sub(and_or(w >> 4, 0x000F000Fu, 0x43004300u), zr), s2r);
+    v[2] = bf16x2_mul(bf16x2_sub(and_or(w >> 8, 0x000F000Fu, 0x43004300u), zr8), s2r8);
+    v[3] = bf16x2_mul(bf16x2_sub(and_or(w >> 12, 0x000F000Fu, 0x43004300u), zr8), s2r8);
+}
+
+template <int NP>
+__global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
+{
+    constexpr int S = ut_stages<NP>();
+    constexpr int SB = ut_stage_bytes<NP>();
+    constexpr uint32_t IDESC = idesc_bf16_f32(128, NP);
+    constexpr int XB = NP * 512;  // activation bytes of one stage
+
+    extern __shared__ uint8_t ut_dsmem[];
+    __shared__ __align__(8) uint64_t bars[2 * S + 2 * UT_NA + 5];
+    __shared__ uint32_t tmem_slot;
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(ut_dsmem) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const long long u0 = ut_range_begin(p, c);
+    const long long u1 = (c + 1 < p.P) ? ut_range_begin(p, c + 1) : p.U;
+    const int n_iter = (int)(u1 - u0);
+    const int gp_first = (int)(u0 / p.KB), b_first = (int)(u0 % p.KB);
+
+    const uint32_t full0 = smem_addr(&bars[0]);
+    const uint32_t empty0 = smem_addr(&bars[S]);
+    const uint32_t afull0 = smem_addr(&bars[2 * S]);
+    const uint32_t aempty0 = smem_addr(&bars[2 * S + UT_NA]);
+    const uint32_t dfull0 = smem_addr(&bars[2 * S + 2 * UT_NA]);       // [2]
+    const uint32_t dempty0 = smem_addr(&bars[2 * S + 2 * UT_NA + 2]);  // [2]
+    const uint32_t mdone = smem_addr(&bars[2 * S + 2 * UT_NA + 4]);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, UT_DQ_WARPS + 2);
+        }
+        for (int k = 0; k < UT_NA; ++k) {
+            mbar_init(afull0 + 8 * k, UT_DQ_WARPS);
+            mbar_init(aempty0 + 8 * k, 2);
+        }
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(dfull0 + 8 * d, 2);
+            mbar_init(dempty0 + 8 * d, UT_EPI_WARPS);
+        }
+        mbar_init(mdone, 2);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&tmem_slot), UT_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0 && n_iter > 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            auto has_g1 = [&](int gp) { return 2 * gp + 1 < p.G; };
+            auto issue_w = [&](int i, int gp, int b) {
+                const int slot = i % S;
+                const uint32_t bar = full0 + 8 * slot;
+                const uint32_t dst = smem_addr(smem + slot * SB + XB);
+                const bool g1 = has_g1(gp);
+                mbar_arrive_expect_tx(bar, (uint32_t)(XB + (g1 ? 2 : 1) * UT_GROUP_BYTES));
+                bulk_g2s(dst, p.packed + ((size_t)(2 * gp) * p.KB + b) * UT_GROUP_BYTES,
+                         UT_GROUP_BYTES, bar, pol_w);
+                if (g1)
+                    bulk_g2s(dst + UT_GROUP_BYTES,
+                             p.packed + ((size_t)(2 * gp + 1) * p.KB + b) * UT_GROUP_BYTES,
+                             UT_GROUP_BYTES, bar, pol_w);
+            };
+            auto issue_x = [&](int i, int b) {
+                const int slot = i % S;
+                bulk_g2s(smem_addr(smem + slot * SB), p.xs + (size_t)b * XB, XB,
+                         full0 + 8 * slot, pol_x);
+            };
+            const int pro = n_iter < S ? n_iter : S;
+            int gp = gp_first, b = b_first;
+            for (int i = 0; i < pro; ++i) {
+                issue_w(i, gp, b);
+                if (++b == p.KB) {
+                    b = 0;
+                    ++gp;
+                }
+            }
+            pdl_wait();  // x comes from act_prep, launched just before
+            int xb = b_first;
+            for (int i = 0; i < pro; ++i) {
+                issue_x(i, xb);
+                if (++xb == p.KB)
+                    xb = 0;
+            }
+            int issued = pro;
+            for (int i = pro; i < n_iter; ++i) {
+                const int slot = i % S;
+                if (!mbar_wait_bounded(empty0 + 8 * slot, (uint32_t)((i / S) - 1) & 1u)) {
+                    report_error(p.err, ERR_EMPTY_WAIT);
+                    break;
+                }
+                issue_w(i, gp, b);
+                issue_x(i, b);
+                issued = i + 1;
+                if (++b == p.KB) {
+                    b = 0;
+                    ++gp;
+                }
+            }
+            // drain: every issued copy has landed before the CTA exits
+            for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+                if (!mbar_wait_bounded(full0 + 8 * (i % S), (uint32_t)(i / S) & 1u)) {
+                    report_error(p.err, ERR_DRAIN_WAIT);
+                    break;
+                }
+        }
+    } else if (warp == 1 || warp == UT_MMA1) {
+        // ------------------------------------------------------ MMA issuers
+        // One thread per tile group of the pair: a single issuing thread
+        // tops out near 47 cycles per N = 64 instruction, two keep the
+        // tensor core at its 32.  Group 1's thread commits (with nothing to
+        // wait for) even when the pair has no group 1, so every barrier
+        // still receives both arrivals.
+        const int gi = warp == 1 ? 0 : 1;
+        if (lane == 0 && n_iter > 0) {
+            int a_it = 0, d_it = 0, gp = gp_first, b = b_first;
+            bool first = true, ok = true;
+            for (int i = 0; i < n_iter && ok; ++i) {
+                const int slot = i % S;
+                if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / S) & 1u) ||
+                    (first && !mbar_wait_bounded(dempty0 + 8 * (d_it & 1),
+                                                 (uint32_t)((d_it >> 1) & 1) ^ 1u))) {
+                    report_error(p.err, ERR_FULL_WAIT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const bool live = gi == 0 || 2 * gp + 1 < p.G;
+                const uint32_t d_tmem = tmem + UT_DCOL * (uint32_t)(d_it & 1) + (uint32_t)(gi * NP);
+                const uint64_t bdesc = sdesc_sw128_kmajor(smem_addr(smem + slot * SB));
+                for (int sbk = 0; sbk < 4; ++sbk) {
+                    const int k = a_it % UT_NA;
+                    if (!mbar_wait_bounded(afull0 + 8 * k, (uint32_t)(a_it / UT_NA) & 1u)) {
+                        report_error(p.err, ERR_FULL_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    if (live) {
+                        const uint32_t a_tmem = tmem + UT_ACOL + (uint32_t)(64 * k + 32 * gi);
+                        // the start-address field (bits 0..13, bytes / 16) advances
+                        // by one sub-block of rows, then by 32 bytes per K step
+                        const uint64_t bd = bdesc + (uint64_t)((sbk * NP * 128) >> 4);
+                        umma_ts(d_tmem, a_tmem, bd, IDESC, (first && sbk == 0) ? 0u : 1u);
+                        umma_ts(d_tmem, a_tmem + 8, bd + 2, IDESC, 1u);
+                        umma_ts(d_tmem, a_tmem + 16, bd + 4, IDESC, 1u);
+                        umma_ts(d_tmem, a_tmem + 24, bd + 6, IDESC, 1u);
+                    }
+                    umma_commit(aempty0 + 8 * k);
+                    ++a_it;
+                }
+                if (!ok)
+                    break;
+                umma_commit(empty0 + 8 * slot);
+                first = false;
+                if (++b == p.KB || i == n_iter - 1) {  // the pair's last unit in this range
+                    umma_commit(dfull0 + 8 * (d_it & 1));
+                    ++d_it;
+                    first = true;
+                    b = 0;
+                    ++gp;
+                }
+            }
+            // every MMA this CTA issued has completed before TMEM is freed
+            umma_commit(mdone);
+            if (!mbar_wait_bounded(mdone, 0u))
+                report_error(p.err, ERR_DRAIN_WAIT);
+        }
+    } else if (warp < UT_FIRST_DQ) {
+        // --------------------------------------------------------- epilogue
+        pdl_wait();  // the arrival counters are zeroed by act_prep
+        const int q = warp & 3;
+        const int L = 32 * q + lane;  // TMEM lane = row within the tile group
+        const size_t seg = (size_t)p.M * UT_PAIR_ROWS;
+        const int gp_last = n_iter > 0 ? (int)((u1 - 1) / p.KB) : gp_first - 1;
+        for (int gp = gp_first, d = 0; gp <= gp_last; ++gp, ++d) {
+            if (!mbar_wait_sleep(dfull0 + 8 * (d & 1), (uint32_t)(d >> 1) & 1u)) {
+                report_error(p.err, ERR_FULL_WAIT);
+                break;
+            }
+            tc_fence_after_sync();
+            const int ng = (2 * gp + 1 < p.G) ? 2 : 1;
+            const long long gb = (long long)gp * p.KB, ge = gb + p.KB;
+            const bool whole = gb >= u0 && ge <= u1;
+            const int slot = (gp == gp_first) ? 0 : 1;
+            for (int gi = 0; gi < ng; ++gi) {
+                uint32_t r[NP / 8][8];
+#pragma unroll
+                for (int ch = 0; ch < NP / 8; ++ch)
+                    tmem_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + UT_DCOL * (uint32_t)(d & 1) +
+                                          (uint32_t)(gi * NP + 8 * ch),
+                                      r[ch]);
+                tmem_wait_ld();
+                float v[NP];
+#pragma unroll
+                for (int ch = 0; ch < NP / 8; ++ch)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        v[8 * ch + j] = __uint_as_float(r[ch][j]);
+                const int n = (2 * gp + gi) * 128 + L;
+                if (whole) {
+                    if (n < p.N) {
+#pragma unroll
+                        for (int m = 0; m < NP; ++m)
+                            if (m < p.M)
+                                p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v[m]);
+                    }
+                } else {
+                    float *dst = p.partial + (size_t)(c * 2 + slot) * seg + (size_t)gi * 128 + L;
+#pragma unroll
+                    for (int m = 0; m < NP; ++m)
+                        if (m < p.M)
+                            dst[(size_t)m * UT_PAIR_ROWS] = v[m];
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(dempty0 + 8 * (d & 1));
+            if (whole)
+                continue;
+            // shared pair: count this warp's arrival per group; the last
+            // contributor sums all partials in CTA order
+            const int cf = ut_range_owner(p, gb), cl = ut_range_owner(p, ge - 1);
+            const int slot0 = (ut_range_begin(p, cf) == gb) ? 0 : 1;
+            const int nc = cl - cf + 1;
+            for (int gi = 0; gi < ng; ++gi) {
+                unsigned last = 0;
+                __syncwarp();  // the warp's partial writes are ordered before lane 0's release
+                if (lane == 0)
+                    last = (atomic_add_acq_rel(&p.counters[(size_t)gp * 8 + gi * 4 + q], 1u) ==
+                            (unsigned)(nc - 1));
+                last = __shfl_sync(0xffffffffu, last, 0);
+                __syncwarp();  // lane 0's acquire is ordered before every lane's reads
+                if (!last)
+                    continue;
+                const int n = (2 * gp + gi) * 128 + L;
+                if (n >= p.N)
+                    continue;
+                const size_t off = (size_t)gi * 128 + L;
+                const float *first = p.partial + (size_t)(cf * 2 + slot0) * seg + off;
+                const float *rest = p.partial + (size_t)(cf * 2 + 2) * seg + off;  // slot 0 of cf+1..
+                // 32 rows of x at a time: every contributor's 32 values are
+                // loaded together, then added in CTA order
+                constexpr int MC = NP < 32 ? NP : 32;
+#pragma unroll
+                for (int m0 = 0; m0 < NP; m0 += MC) {
+                    if (m0 >= p.M)
+                        break;
+                    float acc[MC];
+#pragma unroll
+                    for (int m = 0; m < MC; ++m)
+                        acc[m] = (m0 + m < p.M) ? __ldcg(first + (size_t)(m0 + m) * UT_PAIR_ROWS) : 0.f;
+                    for (int j = 0; j + 1 < nc; ++j) {
+                        const float *src = rest + (size_t)j * 2 * seg;
+                        float t[MC];
+#pragma unroll
+                        for (int m = 0; m < MC; ++m)
+                            t[m] = (m0 + m < p.M) ? __ldcg(src + (size_t)(m0 + m) * UT_PAIR_ROWS) : 0.f;
+#pragma unroll
+                        for (int m = 0; m < MC; ++m)
+                            acc[m] += t[m];
+                    }
+#pragma unroll
+                    for (int m = 0; m < MC; ++m)
+                        if (m0 + m < p.M)
+                            p.out[(size_t)(m0 + m) * p.N + n] = __float2bfloat16_rn(acc[m]);
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- dequant
+        const int q = warp & 3, half = (warp - UT_FIRST_DQ) >> 2;
+        const int tl = 2 * q + half;                          // tile of the group
+        const uint32_t tlane = (uint32_t)(16 * tl) << 16;    // its 16 TMEM lanes
+        const int r = lane >> 2;
+        // The stores of a sub-block complete while the next one is dequantized:
+        // slot `pend` is published (wait::st, then afull) one step later.
+        int a_it = 0, gp = gp_first, b = b_first, pend = -1;
+        bool ok = true;
+        for (int i = 0; i < n_iter && ok; ++i) {
+            const int slot = i % S;
+            if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / S) & 1u)) {
+                report_error(p.err, ERR_FULL_WAIT);
+                break;
+            }
+            const int ng = (2 * gp + 1 < p.G) ? 2 : 1;
+            const uint32_t tbase = smem_addr(smem + slot * SB + XB + tl * UT_TILE_BYTES);
+            uint4 wq[2][4], sc0[2], sc1[2], zz[2];
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi)
+                if (gi < ng) {
+                    const uint32_t tb = tbase + (uint32_t)(gi * UT_GROUP_BYTES);
+#pragma unroll
+                    for (int sbk = 0; sbk < 4; ++sbk)
+                        wq[gi][sbk] = lds128(tb + 512 * sbk + 16 * lane);
+                    sc0[gi] = lds128(tb + 2048 + 16 * r);
+                    sc1[gi] = lds128(tb + 2048 + 128 + 16 * r);
+                    zz[gi] = lds128(tb + 2304 + 16 * r);
+                }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8 * slot);  // the stage's codes are in registers
+#pragma unroll
+            for (int sbk = 0; sbk < 4; ++sbk) {
+                uint32_t v[2][16];
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi)
+                    if (gi < ng) {
+                        const uint32_t scw[8] = {sc0[gi].x, sc0[gi].y, sc0[gi].z, sc0[gi].w,
+                                                 sc1[gi].x, sc1[gi].y, sc1[gi].z, sc1[gi].w};
+                        const uint32_t zw[4] = {zz[gi].x, zz[gi].y, zz[gi].z, zz[gi].w};
+                        const uint32_t wv[4] = {wq[gi][sbk].x, wq[gi][sbk].y, wq[gi][sbk].z,
+                                                wq[gi][sbk].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int g = 2 * sbk + (j >> 1);     // group of 32 within the stage
+                            const uint32_t zsrc = zw[g >> 1];
+                            const uint32_t zb = (uint32_t)((2 * g) & 3);  // z[r][g]; z[r+8][g] next
+                            const uint32_t sp = scw[g];
+                            // (128 + z) in both bf16 halves, rows r and r + 8; (s, s) likewise
+                            const uint32_t zr = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * zb);
+                            const uint32_t zr8 = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * (zb + 1));
+                            const uint32_t s2r = prmt(sp, sp, 0x1010u), s2r8 = prmt(sp, sp, 0x3232u);
+                            ut_dequant_word(wv[j], zr, zr8, s2r, s2r8, &v[gi][4 * j]);
+                        }
+                    }
+                if (pend >= 0) {
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(afull0 + 8 * pend);
+                    pend = -1;
+                }
+                const int k = a_it % UT_NA;
+                if (!mbar_wait_bounded(aempty0 + 8 * k, ((uint32_t)(a_it / UT_NA) & 1u) ^ 1u)) {
+                    report_error(p.err, ERR_EMPTY_WAIT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi)
+                    if (gi < ng)
+                        tmem_st_16x256b_x4(tmem + tlane + UT_ACOL + (uint32_t)(64 * k + 32 * gi),
+                                           v[gi]);
+                pend = k;
+                ++a_it;
+            }
+            if (++b == p.KB) {
+                b = 0;
+                ++gp;
+            }
+        }
+        if (pend >= 0) {
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(afull0 + 8 * pend);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, UT_TMEM_COLS);
+    }
+}
+
+// x -> the B operand layout, plus the zeroing of the arrival counters.
+// One thread per (super-block b, sub-block, row < NP, 16-column step j): the
+// step's eight column pairs w0..w7 are stored in the order
+// w0 w4 w1 w5 | w2 w6 w3 w7 (the column order of the 16x256b TMEM stores of
+// A) as two 16-byte chunks 2j, 2j + 1 of the row's 128-byte line, each at
+// chunk position (chunk ^ row % 8).  Rows >= M are written as zeros.
+__global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                            int M, int K, int NP,
+                                                            uint8_t *__restrict__ xs,
+                                                            unsigned *__restrict__ counters,
+                                                            int ncounters)
+{
+    pdl_launch_dependents();  // the main kernel may start streaming weights
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    for (int i = tid; i < ncounters; i += gridDim.x * blockDim.x)
+        counters[i] = 0u;
+    const long long pieces = (long long)(K / 64) * NP * 4;
+    if (tid >= pieces)
+        return;
+    const int j = tid & 3;
+    const int row = (tid >> 2) % NP;
+    const int bs = (tid >> 2) / NP;  // b * 4 + sub-block
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+    if (row < M) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)row * K + bs * 64 + j * 16);
+        const uint4 a = src[0], b = src[1];
+        lo = make_uint4(a.x, b.x, a.y, b.y);
+        hi = make_uint4(a.z, b.z, a.w, b.w);
+    }
+    uint8_t *line = xs + ((size_t)bs * NP + row) * 128;
+    const int r8 = row & 7;
+    *reinterpret_cast<uint4 *>(line + ((2 * j) ^ r8) * 16) = lo;
+    *reinterpret_cast<uint4 *>(line + ((2 * j + 1) ^ r8) * 16) = hi;
+}
+
+template <int NP>
+cudaError_t launch_umma_np(const UParams &p, cudaStream_t stream)
+{
+    auto fn = w4_umma_kernel<NP>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         ut_smem<NP>());
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.P);
+    cfg.blockDim = dim3(UT_THREADS);
+    cfg.dynamicSmemBytes = ut_smem<NP>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+size_t ut_align(size_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace: [x operand (K/256) * NP * 512][counters G2 * 8][partials P * 2 * M * 256 fp32].
+struct UtLayout {
+    size_t xs, counters, partial, total;
+};
+
+UtLayout ut_layout(const W4Plan &pl)
+{
+    UtLayout L;
+    size_t o = 0;
+    L.xs = o;
+    o += ut_align((size_t)pl.KB * pl.NP * 512);
+    L.counters = o;
+    o += pl.fixup ? ut_align((size_t)pl.G2 * 8 * 4) : 0;
+    L.partial = o;
+    o += pl.partial_bytes;
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+
+size_t w4_umma_workspace(const W4Plan &plan) { return ut_layout(plan).total; }
+
+size_t w4_umma_partial_bytes(int P, int M) { return (size_t)P * 2 * M * UT_PAIR_ROWS * sizeof(float); }
+
+cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed, void *out,
+                           void *workspace, unsigned *err, cudaStream_t stream)
+{
+    const UtLayout L = ut_layout(plan);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    UParams p = {};
+    p.packed = static_cast<const uint8_t *>(packed);
+    p.xs = ws + L.xs;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.partial = reinterpret_cast<float *>(ws + L.partial);
+    p.counters = reinterpret_cast<unsigned *>(ws + L.counters);
+    p.err = err;
+    p.M = plan.M;
+    p.N = plan.N;
+    p.K = plan.K;
+    p.KB = plan.KB;
+    p.G = plan.G;
+    p.G2 = plan.G2;
+    p.P = plan.P;
+    p.split = plan.split;
+    p.U = (long long)plan.G2 * plan.KB;
+    const int ncounters = plan.fixup ? plan.G2 * 8 : 0;
+    const long long pieces = (long long)(plan.K / 64) * plan.NP * 4;
+    const int blocks = (int)((pieces + 255) / 256);
+    act_prep_umma_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                      plan.M, plan.K, plan.NP, ws + L.xs,
+                                                      p.counters, ncounters);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    switch (plan.NP) {
+    case 16: return launch_umma_np<16>(p, stream);
+    case 32: return launch_umma_np<32>(p, stream);
+    case 48: return launch_umma_np<48>(p, stream);
+    default: return launch_umma_np<64>(p, stream);
+    }
+}
+
+}  // namespace w4q

@@ -64,7 +64,7 @@ def test_every_legal_split_matches(cuda):
     N, K = 256, 4096
     W, q, s, z = quantized(N, K, seed=91)
     packed = w4q.w4_pack_weights(W.to(cuda))
-    for M in (1, 2, 3, 4, 16):
+    for M in (1, 2, 3, 4, 16, 17, 40, 64):
         x = workloads.activation(M, K, seed=100 + M)
         ref = oracle.w4a16(x, q, s, z)
         for split in (0, 1, 2, 3, 4, 5, 7, 8, 16):
