@@ -218,8 +218,9 @@ int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8)
     w4q::W4Plan plan;
     if (!w4q::w4_plan((int)M, (int)N, (int)K, -1, sm_count(dev), mode, &plan))
         return -1;
-    (void)plan;
-    return 2;  // the activation preparation (and counter reset), then the main kernel
+    // the activation preparation (and counter reset), the main kernel, and
+    // for the tensor-core kernel with split row groups the partial-sum launch
+    return (plan.umma && plan.fixup) ? 3 : 2;
 }
 
 int w4a16_gemm(const void *x_bf16, const void *packed, void *out_bf16, int64_t M, int64_t N,

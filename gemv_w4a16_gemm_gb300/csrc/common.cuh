@@ -103,10 +103,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// A wait expected to be long (an epilogue waiting for a whole K range):
-// sleeping polls of at most 20 us each, false after WAIT_LIMIT_NS.
+// Wait for the phase of `parity`, the thread sleeping in the instruction
+// (at most 20 us per poll) instead of spinning, so waiting warps leave the
+// issue slots to the others; false after WAIT_LIMIT_NS.
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity)
 {
+    if (mbar_try_wait(bar, parity))
+        return true;
     const unsigned long long t0 = global_timer();
     while (!mbar_try_wait_sleep(bar, parity, 20000u))
         if (global_timer() - t0 > WAIT_LIMIT_NS)

@@ -30,10 +30,14 @@
 // groups (256 rows) x one 256-K super-block: both groups share one copy of
 // the activation stage.  Units are split into P contiguous ranges (stream-K,
 // or a fixed split of each pair's K); a pair that one CTA covers entirely is
-// written directly, the others go through fp32 partials, a per-(pair, group,
-// lane quarter) arrival counter, and an in-order sum by the last arriver.
+// written directly, the others through fp32 partials that a third launch
+// (umma_fixup_kernel, started by programmatic dependent launch as the main
+// kernel's CTAs finish) sums in CTA order: a last-arriver sum inside the main
+// kernel would leave M x (contributors) dependent L2 round trips per thread
+// at the tail of the kernel.
 //
-// Pipelines (every wait bounded by one second of %globaltimer):
+// Pipelines (every wait sleeps in mbarrier.try_wait and gives up after one
+// second of %globaltimer):
 //   producer --full[s]--> dequant + MMA      (packed codes and x of stage s)
 //   dequant  --empty[s]-> producer           (codes read into registers)
 //   MMA      --empty[s]-> producer           (tcgen05.commit: x no longer read)
@@ -55,11 +59,15 @@ constexpr int UT_TILE_BYTES = 2432;               // 16 rows x 256 K: codes, sca
 constexpr int UT_GROUP_BYTES = 8 * UT_TILE_BYTES; // one tile group at one super-block
 constexpr int UT_PAIR_ROWS = 256;
 constexpr int UT_EPI_WARPS = 4;
-constexpr int UT_DQ_WARPS = 8;
+#ifndef W4Q_UMMA_DQ_WARPS
+#define W4Q_UMMA_DQ_WARPS 8
+#endif
+constexpr int UT_DQ_WARPS = W4Q_UMMA_DQ_WARPS;   // 8: two groups per warp, 16: one
+constexpr int UT_GPW = 16 / UT_DQ_WARPS;         // tile groups per dequant warp
 constexpr int UT_FIRST_EPI = 2;
 constexpr int UT_FIRST_DQ = UT_FIRST_EPI + UT_EPI_WARPS;
 constexpr int UT_MMA1 = UT_FIRST_DQ + UT_DQ_WARPS;             // MMA issuer of group 1
-constexpr int UT_THREADS = (UT_MMA1 + 1) * 32;                  // 480
+constexpr int UT_THREADS = (UT_MMA1 + 1) * 32;
 constexpr int UT_NA = 4;             // A slots (one 64-K sub-block of both groups each)
 constexpr uint32_t UT_TMEM_COLS = 512;
 constexpr uint32_t UT_DCOL = 128;    // columns per accumulator buffer (2 groups x NP <= 128)
@@ -71,7 +79,6 @@ struct UParams {
     const uint8_t *xs;       // [K/256][4][NP][128 B]: swizzled, K-permuted x (act_prep)
     __nv_bfloat16 *out;      // bf16 [M][N]
     float *partial;          // fp32 [P][2][M][256]
-    unsigned *counters;      // [G2][8] arrivals per (pair, group, lane quarter)
     unsigned *err;
     int M, N, K, KB, G, G2, P, split;
     long long U;
@@ -107,7 +114,7 @@ __host__ __device__ __forceinline__ long long ut_range_begin(const UParams &p, i
 }
 
 // The CTA whose range holds unit u (the largest c with begin(c) <= u).
-__device__ __forceinline__ int ut_range_owner(const UParams &p, long long u)
+__host__ __device__ __forceinline__ int ut_range_owner(const UParams &p, long long u)
 {
     if (p.split == 0)
         return (int)(((u + 1) * p.P - 1) / p.U);
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             int issued = pro;
             for (int i = pro; i < n_iter; ++i) {
                 const int slot = i % S;
-                if (!mbar_wait_bounded(empty0 + 8 * slot, (uint32_t)((i / S) - 1) & 1u)) {
+                if (!mbar_wait_sleep(empty0 + 8 * slot, (uint32_t)((i / S) - 1) & 1u)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
                 }
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             }
             // drain: every issued copy has landed before the CTA exits
             for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-                if (!mbar_wait_bounded(full0 + 8 * (i % S), (uint32_t)(i / S) & 1u)) {
+                if (!mbar_wait_sleep(full0 + 8 * (i % S), (uint32_t)(i / S) & 1u)) {
                     report_error(p.err, ERR_DRAIN_WAIT);
                     break;
                 }
@@ -257,8 +264,8 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             bool first = true, ok = true;
             for (int i = 0; i < n_iter && ok; ++i) {
                 const int slot = i % S;
-                if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / S) & 1u) ||
-                    (first && !mbar_wait_bounded(dempty0 + 8 * (d_it & 1),
+                if (!mbar_wait_sleep(full0 + 8 * slot, (uint32_t)(i / S) & 1u) ||
+                    (first && !mbar_wait_sleep(dempty0 + 8 * (d_it & 1),
                                                  (uint32_t)((d_it >> 1) & 1) ^ 1u))) {
                     report_error(p.err, ERR_FULL_WAIT);
                     ok = false;
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                 const uint64_t bdesc = sdesc_sw128_kmajor(smem_addr(smem + slot * SB));
                 for (int sbk = 0; sbk < 4; ++sbk) {
                     const int k = a_it % UT_NA;
-                    if (!mbar_wait_bounded(afull0 + 8 * k, (uint32_t)(a_it / UT_NA) & 1u)) {
+                    if (!mbar_wait_sleep(afull0 + 8 * k, (uint32_t)(a_it / UT_NA) & 1u)) {
                         report_error(p.err, ERR_FULL_WAIT);
                         ok = false;
                         break;
@@ -303,12 +310,11 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             }
             // every MMA this CTA issued has completed before TMEM is freed
             umma_commit(mdone);
-            if (!mbar_wait_bounded(mdone, 0u))
+            if (!mbar_wait_sleep(mdone, 0u))
                 report_error(p.err, ERR_DRAIN_WAIT);
         }
     } else if (warp < UT_FIRST_DQ) {
         // --------------------------------------------------------- epilogue
-        pdl_wait();  // the arrival counters are zeroed by act_prep
         const int q = warp & 3;
         const int L = 32 * q + lane;  // TMEM lane = row within the tile group
         const size_t seg = (size_t)p.M * UT_PAIR_ROWS;
@@ -324,93 +330,48 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             const bool whole = gb >= u0 && ge <= u1;
             const int slot = (gp == gp_first) ? 0 : 1;
             for (int gi = 0; gi < ng; ++gi) {
-                uint32_t r[NP / 8][8];
-#pragma unroll
-                for (int ch = 0; ch < NP / 8; ++ch)
-                    tmem_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + UT_DCOL * (uint32_t)(d & 1) +
-                                          (uint32_t)(gi * NP + 8 * ch),
-                                      r[ch]);
-                tmem_wait_ld();
-                float v[NP];
-#pragma unroll
-                for (int ch = 0; ch < NP / 8; ++ch)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        v[8 * ch + j] = __uint_as_float(r[ch][j]);
                 const int n = (2 * gp + gi) * 128 + L;
-                if (whole) {
-                    if (n < p.N) {
+                float *dst = p.partial + (size_t)(c * 2 + slot) * seg + (size_t)gi * 128 + L;
+                // 32 accumulator columns (rows of x) at a time
+                constexpr int CC = NP < 32 ? NP : 32;
 #pragma unroll
-                        for (int m = 0; m < NP; ++m)
-                            if (m < p.M)
-                                p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v[m]);
+                for (int c0 = 0; c0 < NP; c0 += CC) {
+                    uint32_t r[CC / 8][8];
+#pragma unroll
+                    for (int ch = 0; ch < CC / 8; ++ch)
+                        tmem_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) +
+                                              UT_DCOL * (uint32_t)(d & 1) +
+                                              (uint32_t)(gi * NP + c0 + 8 * ch),
+                                          r[ch]);
+                    tmem_wait_ld();
+                    if (c0 >= p.M)
+                        continue;
+                    if (whole) {
+                        if (n < p.N) {
+#pragma unroll
+                            for (int m = 0; m < CC; ++m)
+                                if (c0 + m < p.M)
+                                    p.out[(size_t)(c0 + m) * p.N + n] =
+                                        __float2bfloat16_rn(__uint_as_float(r[m / 8][m % 8]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < CC; ++m)
+                            if (c0 + m < p.M)
+                                dst[(size_t)(c0 + m) * UT_PAIR_ROWS] = __uint_as_float(r[m / 8][m % 8]);
                     }
-                } else {
-                    float *dst = p.partial + (size_t)(c * 2 + slot) * seg + (size_t)gi * 128 + L;
-#pragma unroll
-                    for (int m = 0; m < NP; ++m)
-                        if (m < p.M)
-                            dst[(size_t)m * UT_PAIR_ROWS] = v[m];
                 }
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(dempty0 + 8 * (d & 1));
-            if (whole)
-                continue;
-            // shared pair: count this warp's arrival per group; the last
-            // contributor sums all partials in CTA order
-            const int cf = ut_range_owner(p, gb), cl = ut_range_owner(p, ge - 1);
-            const int slot0 = (ut_range_begin(p, cf) == gb) ? 0 : 1;
-            const int nc = cl - cf + 1;
-            for (int gi = 0; gi < ng; ++gi) {
-                unsigned last = 0;
-                __syncwarp();  // the warp's partial writes are ordered before lane 0's release
-                if (lane == 0)
-                    last = (atomic_add_acq_rel(&p.counters[(size_t)gp * 8 + gi * 4 + q], 1u) ==
-                            (unsigned)(nc - 1));
-                last = __shfl_sync(0xffffffffu, last, 0);
-                __syncwarp();  // lane 0's acquire is ordered before every lane's reads
-                if (!last)
-                    continue;
-                const int n = (2 * gp + gi) * 128 + L;
-                if (n >= p.N)
-                    continue;
-                const size_t off = (size_t)gi * 128 + L;
-                const float *first = p.partial + (size_t)(cf * 2 + slot0) * seg + off;
-                const float *rest = p.partial + (size_t)(cf * 2 + 2) * seg + off;  // slot 0 of cf+1..
-                // 32 rows of x at a time: every contributor's 32 values are
-                // loaded together, then added in CTA order
-                constexpr int MC = NP < 32 ? NP : 32;
-#pragma unroll
-                for (int m0 = 0; m0 < NP; m0 += MC) {
-                    if (m0 >= p.M)
-                        break;
-                    float acc[MC];
-#pragma unroll
-                    for (int m = 0; m < MC; ++m)
-                        acc[m] = (m0 + m < p.M) ? __ldcg(first + (size_t)(m0 + m) * UT_PAIR_ROWS) : 0.f;
-                    for (int j = 0; j + 1 < nc; ++j) {
-                        const float *src = rest + (size_t)j * 2 * seg;
-                        float t[MC];
-#pragma unroll
-                        for (int m = 0; m < MC; ++m)
-                            t[m] = (m0 + m < p.M) ? __ldcg(src + (size_t)(m0 + m) * UT_PAIR_ROWS) : 0.f;
-#pragma unroll
-                        for (int m = 0; m < MC; ++m)
-                            acc[m] += t[m];
-                    }
-#pragma unroll
-                    for (int m = 0; m < MC; ++m)
-                        if (m0 + m < p.M)
-                            p.out[(size_t)(m0 + m) * p.N + n] = __float2bfloat16_rn(acc[m]);
-                }
-            }
         }
     } else {
         // ---------------------------------------------------------- dequant
-        const int q = warp & 3, half = (warp - UT_FIRST_DQ) >> 2;
+        const int dw = warp - UT_FIRST_DQ;
+        const int q = warp & 3, half = (dw >> 2) & 1;
+        const int g0 = UT_GPW == 1 ? (dw >> 3) : 0;          // first group of the pair
         const int tl = 2 * q + half;                          // tile of the group
         const uint32_t tlane = (uint32_t)(16 * tl) << 16;    // its 16 TMEM lanes
         const int r = lane >> 2;
@@ -420,38 +381,38 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
         bool ok = true;
         for (int i = 0; i < n_iter && ok; ++i) {
             const int slot = i % S;
-            if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / S) & 1u)) {
+            if (!mbar_wait_sleep(full0 + 8 * slot, (uint32_t)(i / S) & 1u)) {
                 report_error(p.err, ERR_FULL_WAIT);
                 break;
             }
             const int ng = (2 * gp + 1 < p.G) ? 2 : 1;
             const uint32_t tbase = smem_addr(smem + slot * SB + XB + tl * UT_TILE_BYTES);
-            uint4 wq[2][4], sc0[2], sc1[2], zz[2];
+            uint4 wq[UT_GPW][4], sc0[UT_GPW], sc1[UT_GPW], zz[UT_GPW];
 #pragma unroll
-            for (int gi = 0; gi < 2; ++gi)
-                if (gi < ng) {
-                    const uint32_t tb = tbase + (uint32_t)(gi * UT_GROUP_BYTES);
+            for (int gg = 0; gg < UT_GPW; ++gg)
+                if (g0 + gg < ng) {
+                    const uint32_t tb = tbase + (uint32_t)((g0 + gg) * UT_GROUP_BYTES);
 #pragma unroll
                     for (int sbk = 0; sbk < 4; ++sbk)
-                        wq[gi][sbk] = lds128(tb + 512 * sbk + 16 * lane);
-                    sc0[gi] = lds128(tb + 2048 + 16 * r);
-                    sc1[gi] = lds128(tb + 2048 + 128 + 16 * r);
-                    zz[gi] = lds128(tb + 2304 + 16 * r);
+                        wq[gg][sbk] = lds128(tb + 512 * sbk + 16 * lane);
+                    sc0[gg] = lds128(tb + 2048 + 16 * r);
+                    sc1[gg] = lds128(tb + 2048 + 128 + 16 * r);
+                    zz[gg] = lds128(tb + 2304 + 16 * r);
                 }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * slot);  // the stage's codes are in registers
 #pragma unroll
             for (int sbk = 0; sbk < 4; ++sbk) {
-                uint32_t v[2][16];
+                uint32_t v[UT_GPW][16];
 #pragma unroll
-                for (int gi = 0; gi < 2; ++gi)
-                    if (gi < ng) {
-                        const uint32_t scw[8] = {sc0[gi].x, sc0[gi].y, sc0[gi].z, sc0[gi].w,
-                                                 sc1[gi].x, sc1[gi].y, sc1[gi].z, sc1[gi].w};
-                        const uint32_t zw[4] = {zz[gi].x, zz[gi].y, zz[gi].z, zz[gi].w};
-                        const uint32_t wv[4] = {wq[gi][sbk].x, wq[gi][sbk].y, wq[gi][sbk].z,
-                                                wq[gi][sbk].w};
+                for (int gg = 0; gg < UT_GPW; ++gg)
+                    if (g0 + gg < ng) {
+                        const uint32_t scw[8] = {sc0[gg].x, sc0[gg].y, sc0[gg].z, sc0[gg].w,
+                                                 sc1[gg].x, sc1[gg].y, sc1[gg].z, sc1[gg].w};
+                        const uint32_t zw[4] = {zz[gg].x, zz[gg].y, zz[gg].z, zz[gg].w};
+                        const uint32_t wv[4] = {wq[gg][sbk].x, wq[gg][sbk].y, wq[gg][sbk].z,
+                                                wq[gg][sbk].w};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int g = 2 * sbk + (j >> 1);     // group of 32 within the stage
@@ -462,7 +423,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                             const uint32_t zr = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * zb);
                             const uint32_t zr8 = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * (zb + 1));
                             const uint32_t s2r = prmt(sp, sp, 0x1010u), s2r8 = prmt(sp, sp, 0x3232u);
-                            ut_dequant_word(wv[j], zr, zr8, s2r, s2r8, &v[gi][4 * j]);
+                            ut_dequant_word(wv[j], zr, zr8, s2r, s2r8, &v[gg][4 * j]);
                         }
                     }
                 if (pend >= 0) {
@@ -474,17 +435,17 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                     pend = -1;
                 }
                 const int k = a_it % UT_NA;
-                if (!mbar_wait_bounded(aempty0 + 8 * k, ((uint32_t)(a_it / UT_NA) & 1u) ^ 1u)) {
+                if (!mbar_wait_sleep(aempty0 + 8 * k, ((uint32_t)(a_it / UT_NA) & 1u) ^ 1u)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
 #pragma unroll
-                for (int gi = 0; gi < 2; ++gi)
-                    if (gi < ng)
-                        tmem_st_16x256b_x4(tmem + tlane + UT_ACOL + (uint32_t)(64 * k + 32 * gi),
-                                           v[gi]);
+                for (int gg = 0; gg < UT_GPW; ++gg)
+                    if (g0 + gg < ng)
+                        tmem_st_16x256b_x4(
+                            tmem + tlane + UT_ACOL + (uint32_t)(64 * k + 32 * (g0 + gg)), v[gg]);
                 pend = k;
                 ++a_it;
             }
@@ -502,6 +463,10 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
         }
     }
 
+    // The fixup launch may start once every CTA is here (it waits for the
+    // grid's completion before reading partials); triggering any earlier
+    // would park its blocks, waiting, beside the dequant warps.
+    pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
@@ -510,22 +475,17 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
     }
 }
 
-// x -> the B operand layout, plus the zeroing of the arrival counters.
-// One thread per (super-block b, sub-block, row < NP, 16-column step j): the
+// x -> the B operand layout.  One thread per (super-block b, sub-block, row < NP, 16-column step j): the
 // step's eight column pairs w0..w7 are stored in the order
 // w0 w4 w1 w5 | w2 w6 w3 w7 (the column order of the 16x256b TMEM stores of
 // A) as two 16-byte chunks 2j, 2j + 1 of the row's 128-byte line, each at
 // chunk position (chunk ^ row % 8).  Rows >= M are written as zeros.
 __global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 *__restrict__ x,
                                                             int M, int K, int NP,
-                                                            uint8_t *__restrict__ xs,
-                                                            unsigned *__restrict__ counters,
-                                                            int ncounters)
+                                                            uint8_t *__restrict__ xs)
 {
     pdl_launch_dependents();  // the main kernel may start streaming weights
     const int tid = blockIdx.x * blockDim.x + threadIdx.x;
-    for (int i = tid; i < ncounters; i += gridDim.x * blockDim.x)
-        counters[i] = 0u;
     const long long pieces = (long long)(K / 64) * NP * 4;
     if (tid >= pieces)
         return;
@@ -543,6 +503,68 @@ __global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 
     const int r8 = row & 7;
     *reinterpret_cast<uint4 *>(line + ((2 * j) ^ r8) * 16) = lo;
     *reinterpret_cast<uint4 *>(line + ((2 * j + 1) ^ r8) * 16) = hi;
+}
+
+// Sum of the fp32 partials of the pairs that several CTAs share, in CTA
+// order (deterministic).  Block (pair, 8 rows of x), one thread per pair
+// row: every load of a group of contributors is issued before the in-order
+// sum, so the launch is about one wave of a few L2 round trips.  Launched
+// behind the main kernel with programmatic dependent launch;
+// griddepcontrol.wait holds it until the main kernel has finished.
+constexpr int UT_FIX_ROWS = 8;
+
+__global__ void __launch_bounds__(UT_PAIR_ROWS) umma_fixup_kernel(const UParams p)
+{
+    pdl_wait();
+    const int gp = blockIdx.x, m0 = blockIdx.y * UT_FIX_ROWS, row = threadIdx.x;
+    const long long gb = (long long)gp * p.KB, ge = gb + p.KB;
+    const int cf = ut_range_owner(p, gb), cl = ut_range_owner(p, ge - 1);
+    const int n = gp * UT_PAIR_ROWS + row;
+    if (cf == cl || n >= p.N)
+        return;  // a whole pair: written by the main kernel
+    const size_t seg = (size_t)p.M * UT_PAIR_ROWS;
+    const int slot0 = (ut_range_begin(p, cf) == gb) ? 0 : 1;
+    const float *first = p.partial + (size_t)(cf * 2 + slot0) * seg + (size_t)m0 * UT_PAIR_ROWS + row;
+    const float *rest = p.partial + (size_t)(cf * 2 + 2) * seg + (size_t)m0 * UT_PAIR_ROWS + row;
+    const int nc = cl - cf;  // contributors after cf (slot 0 of cf + 1 ..)
+    float v[UT_FIX_ROWS];
+#pragma unroll
+    for (int r = 0; r < UT_FIX_ROWS; ++r)
+        v[r] = (m0 + r < p.M) ? __ldcg(first + (size_t)r * UT_PAIR_ROWS) : 0.f;
+    for (int j = 0; j < nc; j += 4) {
+        float t[UT_FIX_ROWS][4];
+#pragma unroll
+        for (int r = 0; r < UT_FIX_ROWS; ++r)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                t[r][u] = (m0 + r < p.M && j + u < nc)
+                              ? __ldcg(rest + (size_t)(j + u) * 2 * seg + (size_t)r * UT_PAIR_ROWS)
+                              : 0.f;
+#pragma unroll
+        for (int r = 0; r < UT_FIX_ROWS; ++r)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j + u < nc)
+                    v[r] += t[r][u];
+    }
+#pragma unroll
+    for (int r = 0; r < UT_FIX_ROWS; ++r)
+        if (m0 + r < p.M)
+            p.out[(size_t)(m0 + r) * p.N + n] = __float2bfloat16_rn(v[r]);
+}
+
+cudaError_t launch_fixup(const UParams &p, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.G2, (unsigned)((p.M + UT_FIX_ROWS - 1) / UT_FIX_ROWS));
+    cfg.blockDim = dim3(UT_PAIR_ROWS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, umma_fixup_kernel, p);
 }
 
 template <int NP>
@@ -568,9 +590,9 @@ cudaError_t launch_umma_np(const UParams &p, cudaStream_t stream)
 
 size_t ut_align(size_t v) { return (v + 255) / 256 * 256; }
 
-// Workspace: [x operand (K/256) * NP * 512][counters G2 * 8][partials P * 2 * M * 256 fp32].
+// Workspace: [x operand (K/256) * NP * 512][partials P * 2 * M * 256 fp32].
 struct UtLayout {
-    size_t xs, counters, partial, total;
+    size_t xs, partial, total;
 };
 
 UtLayout ut_layout(const W4Plan &pl)
@@ -579,8 +601,6 @@ UtLayout ut_layout(const W4Plan &pl)
     size_t o = 0;
     L.xs = o;
     o += ut_align((size_t)pl.KB * pl.NP * 512);
-    L.counters = o;
-    o += pl.fixup ? ut_align((size_t)pl.G2 * 8 * 4) : 0;
     L.partial = o;
     o += pl.partial_bytes;
     L.total = o;
@@ -603,7 +623,6 @@ cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed
     p.xs = ws + L.xs;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.partial = reinterpret_cast<float *>(ws + L.partial);
-    p.counters = reinterpret_cast<unsigned *>(ws + L.counters);
     p.err = err;
     p.M = plan.M;
     p.N = plan.N;
@@ -614,21 +633,22 @@ cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed
     p.P = plan.P;
     p.split = plan.split;
     p.U = (long long)plan.G2 * plan.KB;
-    const int ncounters = plan.fixup ? plan.G2 * 8 : 0;
     const long long pieces = (long long)(plan.K / 64) * plan.NP * 4;
     const int blocks = (int)((pieces + 255) / 256);
     act_prep_umma_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                      plan.M, plan.K, plan.NP, ws + L.xs,
-                                                      p.counters, ncounters);
+                                                      plan.M, plan.K, plan.NP, ws + L.xs);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     switch (plan.NP) {
-    case 16: return launch_umma_np<16>(p, stream);
-    case 32: return launch_umma_np<32>(p, stream);
-    case 48: return launch_umma_np<48>(p, stream);
-    default: return launch_umma_np<64>(p, stream);
+    case 16: e = launch_umma_np<16>(p, stream); break;
+    case 32: e = launch_umma_np<32>(p, stream); break;
+    case 48: e = launch_umma_np<48>(p, stream); break;
+    default: e = launch_umma_np<64>(p, stream); break;
     }
+    if (e != cudaSuccess || !plan.fixup)
+        return e;
+    return launch_fixup(p, stream);
 }
 
 }  // namespace w4q

@@ -135,8 +135,10 @@ int w4_split_choice(int64_t M, int64_t N, int64_t K, int group);
 
 /* Number of kernels one w4a16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1) call
  * with these sizes launches on the current device: the activation
- * preparation (W4A8 quantizer / W4A16 power-of-two prescale, split-K
- * counter reset) and the main kernel.  -1 when the sizes are unsupported. */
+ * preparation (W4A8 quantizer / W4A16 power-of-two prescale or tensor-core
+ * operand layout, split-K counter reset) and the main kernel; for W4A16 at
+ * M > 16 with row groups split over several CTAs, also the launch that sums
+ * their fp32 partials.  -1 when the sizes are unsupported. */
 int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
 
 /* out = x . dequant(packed)^T, W4A16.

@@ -97,7 +97,7 @@ def test_every_runtime_m_up_to_64(cuda):
 def test_workspace_too_small_is_rejected(cuda):
     # w4_workspace_bytes covers both W4A16 and W4A8 (the larger, with the
     # int8 activation buffers); a buffer 16 bytes short fails W4A8, and a
-    # 16-byte buffer fails W4A16 when it needs split-K partials.
+    # 16-byte buffer fails W4A16.
     N, K, M = 8448, 6656, 4
     need = w4q.workspace_bytes(M, N, K)
     assert need > 0
@@ -109,10 +109,10 @@ def test_workspace_too_small_is_rejected(cuda):
     with pytest.raises(w4q.W4QError) as e:
         w4q.w4a8_gemm(x, packed, N, K, workspace=small, out=out)
     assert e.value.status == 4
-    if w4q.kernel_launches(M, N, K) > 1:          # a fixup: partials needed
-        with pytest.raises(w4q.W4QError) as e:
-            w4q.w4a16_gemm(x, packed, N, K, workspace=small[:16], out=out)
-        assert e.value.status == 4
+    # W4A16 always needs the prepared activation operand: 16 bytes is short
+    with pytest.raises(w4q.W4QError) as e:
+        w4q.w4a16_gemm(x, packed, N, K, workspace=small[:16], out=out)
+    assert e.value.status == 4
     assert torch.all(out == 3.0)
 
 
