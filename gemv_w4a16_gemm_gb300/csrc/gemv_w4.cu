@@ -6,7 +6,10 @@
 // bucket kernels and the W4A16 tile kernels; this is a new design for GB300,
 // not their code.)
 //
-// Two launches per call:
+// Two launches per call, both with programmatic dependent launch: act_prep
+// starts while the previous kernel on the stream finishes (it waits for it in
+// griddepcontrol.wait before reading x), and the main kernel starts
+// streaming weights while act_prep runs.
 //  1. act_prep (a few CTAs per activation row) prepares the activation operand
 //     in the workspace, super-block-major ([K/256][M][256 + 8 pad] bf16 and
 //     [K/256][M][8] fp32, so one bulk copy moves a stage's rows), and zeroes
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
         }
     }
     __syncthreads();
+    pdl_launch_dependents();  // the next call's preparation may launch and wait
 
     // stage i processes unit u0 + i = (g, b); both sides step (g, b) along
     const int g_first = (int)(u0 / p.KB), b_first = (int)(u0 % p.KB);
@@ -512,6 +516,7 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     int ncounters)
 {
     pdl_launch_dependents();  // the main kernel may start streaming weights
+    pdl_wait();               // x (and this workspace) may belong to the previous kernel
     const int nblk = gridDim.x * gridDim.y;
     const int bid = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = bid * PREP_THREADS + threadIdx.x; i < ncounters; i += nblk * PREP_THREADS)
@@ -827,17 +832,22 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     float *osc = reinterpret_cast<float *>(ws + L.oscale);
     unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.counters);
     const __nv_bfloat16 *xin = static_cast<const __nv_bfloat16 *>(x);
-    const dim3 pgrid((unsigned)plan.M, (unsigned)((plan.K + PREP_CHUNK - 1) / PREP_CHUNK));
-    if (mode == W4Mode::A16 && plan.fold)
-        act_prep_kernel<PREP_COPY><<<pgrid, PREP_THREADS, 0, stream>>>(xin, plan.M, plan.K, xp,
-                                                                       xsum, osc, cnt, ncounters);
-    else if (mode == W4Mode::A16)
-        act_prep_kernel<PREP_A16><<<pgrid, PREP_THREADS, 0, stream>>>(xin, plan.M, plan.K, xp,
-                                                                      xsum, osc, cnt, ncounters);
-    else
-        act_prep_kernel<PREP_A8><<<pgrid, PREP_THREADS, 0, stream>>>(xin, plan.M, plan.K, xp,
-                                                                     xsum, osc, cnt, ncounters);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the preparation launches while the
+    // previous kernel finishes and waits for it in griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.M, (unsigned)((plan.K + PREP_CHUNK - 1) / PREP_CHUNK));
+    cfg.blockDim = dim3(PREP_THREADS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto prep = (mode == W4Mode::A16 && plan.fold) ? act_prep_kernel<PREP_COPY>
+                : (mode == W4Mode::A16)            ? act_prep_kernel<PREP_A16>
+                                                   : act_prep_kernel<PREP_A8>;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prep, xin, plan.M, plan.K, xp, xsum, osc, cnt,
+                                       ncounters);
     if (e != cudaSuccess)
         return e;
     if (mode == W4Mode::A16)

@@ -485,6 +485,7 @@ __global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 
                                                             uint8_t *__restrict__ xs)
 {
     pdl_launch_dependents();  // the main kernel may start streaming weights
+    pdl_wait();               // x (and this workspace) may belong to the previous kernel
     const int tid = blockIdx.x * blockDim.x + threadIdx.x;
     const long long pieces = (long long)(K / 64) * NP * 4;
     if (tid >= pieces)
@@ -635,9 +636,20 @@ cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed
     p.U = (long long)plan.G2 * plan.KB;
     const long long pieces = (long long)(plan.K / 64) * plan.NP * 4;
     const int blocks = (int)((pieces + 255) / 256);
-    act_prep_umma_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                      plan.M, plan.K, plan.NP, ws + L.xs);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the preparation launches while the
+    // previous kernel finishes and waits for it in griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, act_prep_umma_kernel,
+                                       static_cast<const __nv_bfloat16 *>(x), plan.M, plan.K,
+                                       plan.NP, ws + L.xs);
     if (e != cudaSuccess)
         return e;
     switch (plan.NP) {

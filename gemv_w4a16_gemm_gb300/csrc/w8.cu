@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
         fence_barrier_init();
     }
     __syncthreads();
+    pdl_launch_dependents();  // the next call's preparation may launch and wait
 
     int issued = 0;
     if (warp == CWARPS) {
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
             }
         }
     } else {
+        pdl_wait();  // x may come from the kernel launched before this one
         // activations of this lane's columns, fp32, for the whole kernel
         float xr[CH][16][M];
 #pragma unroll
@@ -198,8 +200,19 @@ cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
-    w8_kernel<M, CH, RW><<<p.P, THREADS, smem, stream>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the weight stream starts while the
+    // previous kernel finishes; x is read after griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.P);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, w8_kernel<M, CH, RW>, p);
 }
 
 }  // namespace
