@@ -109,7 +109,7 @@ def call_label(kind, N, K, M):
 def kernel_name(kind, M):
     if kind == "w8":
         return "w8_kernel<M=%d>" % M
-    if kind == "w4a16" and M > 16:
+    if kind == "w4a16" and M >= 9:
         return "w4_umma_kernel<NP=%d>" % ((M + 15) // 16 * 16)
     nb = 1 if M <= 8 else (2 if M <= 16 else (4 if M <= 32 else 8))
     return "w4_kernel<NB=%d,%s>" % (nb, "A8" if kind == "w4a8" else "A16")

@@ -1,4 +1,6 @@
-// gemv_w4.cu -- decode-sized W4A16 / W4A8 linear layer on sm_103a.
+// gemv_w4.cu -- decode-sized W4A16 (M <= 8) / W4A8 linear layer on sm_103a.
+// (W4A16 at M >= 9 is a contraction for the tcgen05 tensor core:
+// gemv_w4_umma.cu.)
 //
 //   out[M,N] = x[M,K] . dequant(Wq)[N,K]^T,   dequant(q) = (q - z) * s
 //
@@ -42,10 +44,6 @@
 //         D - z * X'[g] and the scale as acc += s * (D - z * X'[g]) (fp32).
 //         For W4A8 every product and partial sum is an exact multiple of
 //         2^-12 below 2^12, so the group dot is the exact integer dot.
-//       * For W4A16 at M > 16 the scaled weight (q - z) * s is rounded once
-//         to bf16 (codes via 128-offset bf16 arithmetic) and the MMA
-//         accumulates over all of K on the unscaled x: per-group fp32
-//         scaling would cost more ALU than the tensor core saves.
 //       * Work partition: units (tile group, 256-K super-block) are split
 //         into P contiguous ranges, one per CTA (balanced "stream-K" ranges
 //         over all SM slots by default, or a fixed split of each group's K).
@@ -72,8 +70,8 @@ constexpr int SROW = 32;                   // one activation row's 8 group sums 
 
 struct Params {
     const uint8_t *packed;
-    const __nv_bfloat16 *x;  // bf16 [K/256][M][264]: x' (prepared) or, when folding, x
-    const float *xsum;       // fp32 [K/256][M][8]: X' (not used when folding)
+    const __nv_bfloat16 *x;  // bf16 [K/256][M][264]: x' (prepared)
+    const float *xsum;       // fp32 [K/256][M][8]: X'
     const float *oscale;     // fp32 [M]: output scale per row
     __nv_bfloat16 *out;      // bf16 [M][N]
     int32_t *dots;           // group-dot export: int32 [M][N][K/32]
@@ -101,17 +99,10 @@ __device__ __forceinline__ int range_owner(const Params &p, long long u)
     return g * p.split + (int)(((long long)(b + 1) * p.split - 1) / p.KB);
 }
 
-// The dequantized weight is folded into bf16 for W4A16 at M > 16 (NB >= 4).
-template <int NB, W4Mode MODE>
-__host__ __device__ constexpr bool fold_for()
-{
-    return MODE == W4Mode::A16 && NB >= 4;
-}
-
 template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int stage_bytes()
 {
-    return WARPS * TILE_BYTES + NB * 8 * XROW + (fold_for<NB, MODE>() ? 0 : NB * 8 * SROW);
+    return WARPS * TILE_BYTES + NB * 8 * XROW + NB * 8 * SROW;
 }
 
 template <int NB, W4Mode MODE>
@@ -131,8 +122,8 @@ __host__ __device__ constexpr int smem_for()
 
 // One stage: this warp's 16 x 256 tile, 4 sub-blocks of 64 K (two groups
 // each), 4 k16 steps per sub-block.  xbase: the stage's activation rows;
-// sbase: the stage's group sums (unused when folding).
-template <int NB, bool FOLD, bool DOTS>
+// sbase: the stage's group sums.
+template <int NB, bool DOTS>
 __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, uint32_t sbase,
                                               int lane, float (&acc)[NB][4], const Params &p,
                                               int tile, int b)
@@ -149,7 +140,7 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
 
     // group sums X' of this lane's two output columns, per n8 block
     float xs[NB][2][8];
-    if (!FOLD) {
+    {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
@@ -184,24 +175,7 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
             const uint32_t zsrc = zw[g >> 1];
             const uint32_t zb = (uint32_t)((2 * g) & 3);  // byte of z[r][g]; z[r+8][g] follows
             const uint32_t sp = scw[g];
-            if (FOLD) {
-                // (128 + z) in both bf16 halves, rows r and r + 8
-                const uint32_t zr = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * zb);
-                const uint32_t zr8 = prmt(zsrc, 0x43u, 0x4040u + 0x0101u * (zb + 1));
-                const uint32_t s2r = prmt(sp, sp, 0x1010u), s2r8 = prmt(sp, sp, 0x3232u);
-#pragma unroll
-                for (int st = 0; st < 2; ++st) {
-                    const uint32_t w = wv[2 * gi + st];
-                    uint32_t a[4];  // rows r, r+8 x cols c, c+8 (bits 0, 8, 4, 12)
-                    a[0] = bf16x2_mul(bf16x2_sub(and_or(w, 0x000F000Fu, 0x43004300u), zr), s2r);
-                    a[1] = bf16x2_mul(bf16x2_sub(and_or(w >> 8, 0x000F000Fu, 0x43004300u), zr8), s2r8);
-                    a[2] = bf16x2_mul(bf16x2_sub(and_or(w >> 4, 0x000F000Fu, 0x43004300u), zr), s2r);
-                    a[3] = bf16x2_mul(bf16x2_sub(and_or(w >> 12, 0x000F000Fu, 0x43004300u), zr8), s2r8);
-#pragma unroll
-                    for (int nb = 0; nb < NB; ++nb)
-                        mma_bf16(acc[nb], a, bf[nb][2 * gi + st][0], bf[nb][2 * gi + st][1], acc[nb]);
-                }
-            } else {
+            {
                 float d[NB][4];
 #pragma unroll
                 for (int st = 0; st < 2; ++st) {
@@ -253,7 +227,6 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
 template <int NB, W4Mode MODE>
 __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Params p)
 {
-    constexpr bool FOLD = fold_for<NB, MODE>();
     constexpr bool DOTS = MODE == W4Mode::A8_DOTS;
     constexpr int STAGES = stages_for<NB, MODE>();
     constexpr int SB = stage_bytes<NB, MODE>();
@@ -278,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     }
     {   // activation rows m >= M of every stage stay zero (never copied into)
         const int pad_rows = NB * 8 - p.M;
-        const int xper = pad_rows * (XROW / 16), sper = FOLD ? 0 : pad_rows * (SROW / 16);
+        const int xper = pad_rows * (XROW / 16), sper = pad_rows * (SROW / 16);
         for (int i = threadIdx.x; i < STAGES * (xper + sper); i += THREADS) {
             const int s = i / (xper + sper), rem = i % (xper + sper);
             uint8_t *dst = rem < xper
@@ -300,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             const uint32_t xbytes = (uint32_t)p.M * XROW, sbytes = (uint32_t)p.M * SROW;
-            const uint32_t act_bytes = xbytes + (FOLD ? 0u : sbytes);
+            const uint32_t act_bytes = xbytes + sbytes;
             auto issue_w = [&](int i, int g, int b) {
                 const int slot = i % STAGES;
                 const uint32_t bar = full0 + 8 * slot;
@@ -314,9 +287,8 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 const uint32_t bar = full0 + 8 * slot;
                 bulk_g2s(smem_addr(smem + slot * SB + XOFF),
                          p.x + (size_t)b * p.M * (XROW / 2), xbytes, bar, pol_x);
-                if (!FOLD)
-                    bulk_g2s(smem_addr(smem + slot * SB + SOFF),
-                             p.xsum + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
+                bulk_g2s(smem_addr(smem + slot * SB + SOFF),
+                         p.xsum + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
             };
             // Prologue: two stages of weights go out at once; the activation
             // copies follow as soon as act_prep has finished.  The other
@@ -466,7 +438,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             }
             const int tile = g * WARPS + warp;
             if (tile < p.T)
-                compute_stage<NB, FOLD, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
+                compute_stage<NB, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
                                               smem_addr(smem + slot * SB + XOFF),
                                               smem_addr(smem + slot * SB + SOFF), lane, acc, p,
                                               tile, b);
@@ -498,10 +470,9 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
 
 // Activation preparation (see the file comment), plus the zeroing of the
 // split-K counters.  KIND: PREP_A16 (power-of-two prescale
-// and group sums), PREP_COPY (folded W4A16: x copied as is, scale 1),
-// PREP_A8 (the W4A8 quantizer).  Outputs are super-block-major:
+// and group sums), PREP_A8 (the W4A8 quantizer).  Outputs are super-block-major:
 // xp[(k/256)*M + m][264] (16 pad bytes per row) and xsum[(g/8)*M + m][8].
-enum { PREP_A16 = 0, PREP_COPY = 1, PREP_A8 = 2 };
+enum { PREP_A16 = 0, PREP_A8 = 2 };
 
 constexpr int PREP_THREADS = 256;
 constexpr int PREP_CHUNK = PREP_THREADS * 8;  // columns one CTA transforms
@@ -526,39 +497,36 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
     const int n8 = K / 8;
     float a = 0.f;
-    if (KIND != PREP_COPY) {
-        for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
-            const uint4 v = row[i];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
+        const uint4 v = row[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if ((threadIdx.x & 31) == 0)
-            red[threadIdx.x >> 5] = a;
-        __syncthreads();
-        a = 0.f;
-#pragma unroll
-        for (int i = 0; i < PREP_THREADS / 32; ++i)
-            a = fmaxf(a, red[i]);
+        for (int j = 0; j < 4; ++j)
+            a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = a;
+    __syncthreads();
+    a = 0.f;
+#pragma unroll
+    for (int i = 0; i < PREP_THREADS / 32; ++i)
+        a = fmaxf(a, red[i]);
     float sxm = 0.f;  // W4A8 activation scale
     int sigma = 0;    // x' = value * 2^sigma on lower half-steps (2^(sigma-4) upper)
     if (KIND == PREP_A8) {
         sxm = __fdiv_rn(a, 127.0f);
         sigma = 121;
-    } else if (KIND == PREP_A16) {
+    } else {
         int e = 0;
         if (a > 0.f)
             (void)frexpf(a, &e);  // a < 2^e
         sigma = min(max(128 - e, 6), 259);
     }
     if (threadIdx.x == 0 && blockIdx.y == 0)
-        oscale[m] = KIND == PREP_A8 ? sxm * 4096.0f
-                                    : (KIND == PREP_A16 ? ldexpf(1.0f, 133 - sigma) : 1.0f);
+        oscale[m] = KIND == PREP_A8 ? sxm * 4096.0f : ldexpf(1.0f, 133 - sigma);
     // 8 consecutive values per thread; 4 threads per group of 32
     const int i = blockIdx.y * PREP_THREADS + threadIdx.x;
     const bool live = i < n8;
@@ -566,44 +534,39 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     if (live) {
         const int k0 = 8 * i;
         const uint4 raw = row[i];
-        uint4 o = raw;
-        if (KIND != PREP_COPY) {
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            float v[8];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        float v[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[2 * j] = bf16lo_to_f32(w[j]);
-                v[2 * j + 1] = bf16hi_to_f32(w[j]);
-            }
-            if (KIND == PREP_A8) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxm)), -127.f), 127.f);
-            }
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = bf16lo_to_f32(w[j]);
+            v[2 * j + 1] = bf16hi_to_f32(w[j]);
+        }
+        if (KIND == PREP_A8) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                part += v[j];
-            // columns 8i .. 8i+7: upper half of a 16-column step when i is odd
-            const int sh = (i & 1) ? sigma - 4 : sigma;
-            uint32_t ow[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                ow[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j], sh))) |
-                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j + 1], sh)))
-                         << 16);
-            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxm)), -127.f), 127.f);
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            part += v[j];
+        // columns 8i .. 8i+7: upper half of a 16-column step when i is odd
+        const int sh = (i & 1) ? sigma - 4 : sigma;
+        uint32_t ow[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            ow[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j], sh))) |
+                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ldexpf(v[2 * j + 1], sh)))
+                     << 16);
+        const uint4 o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
         const size_t dst = ((size_t)(k0 / 256) * M + m) * 264 + (k0 % 256);
         *reinterpret_cast<uint4 *>(xp + dst) = o;
     }
-    if (KIND != PREP_COPY) {
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (live && (i & 3) == 0) {
-            const int g = i / 4;
-            xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] =
-                ldexpf(part, KIND == PREP_A8 ? -12 : sigma - 133);
-        }
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    if (live && (i & 3) == 0) {
+        const int g = i / 4;
+        xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] =
+            ldexpf(part, KIND == PREP_A8 ? -12 : sigma - 133);
     }
 }
 
@@ -732,7 +695,7 @@ WsLayout ws_layout(const W4Plan &pl)
     L.xp = o;
     o += align_up((size_t)pl.KB * pl.M * XROW, 256);
     L.xsum = o;
-    o += pl.fold ? 0 : align_up((size_t)pl.KB * pl.M * SROW, 256);
+    o += align_up((size_t)pl.KB * pl.M * SROW, 256);
     L.oscale = o;
     o += align_up((size_t)pl.M * 4, 256);
     L.counters = o;
@@ -757,8 +720,11 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     pl.T = (N + 15) / 16;
     pl.G = (pl.T + WARPS - 1) / WARPS;
     pl.NB = nb_for(M);
-    pl.fold = (mode == W4Mode::A16) && M > 16;
-    pl.umma = pl.fold;  // W4A16 above 16 rows runs on the tcgen05 tensor core
+#ifndef W4Q_UMMA_MIN_M
+#define W4Q_UMMA_MIN_M 9
+#endif
+    pl.umma = (mode == W4Mode::A16) && M >= W4Q_UMMA_MIN_M;  // W4A16 on the tcgen05 tensor core
+    pl.fold = pl.umma;  // the dequantized weight is rounded to bf16 there
     pl.NP = (M + 15) / 16 * 16;
     pl.G2 = (pl.G + 1) / 2;
     const int groups = pl.umma ? pl.G2 : pl.G;  // work-unit rows: tile groups or pairs
@@ -843,9 +809,7 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    auto prep = (mode == W4Mode::A16 && plan.fold) ? act_prep_kernel<PREP_COPY>
-                : (mode == W4Mode::A16)            ? act_prep_kernel<PREP_A16>
-                                                   : act_prep_kernel<PREP_A8>;
+    auto prep = mode == W4Mode::A16 ? act_prep_kernel<PREP_A16> : act_prep_kernel<PREP_A8>;
     cudaError_t e = cudaLaunchKernelEx(&cfg, prep, xin, plan.M, plan.K, xp, xsum, osc, cnt,
                                        ncounters);
     if (e != cudaSuccess)

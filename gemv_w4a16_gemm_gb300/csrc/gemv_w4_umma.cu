@@ -1,4 +1,4 @@
-// gemv_w4_umma.cu -- W4A16 linear layer for 16 < M <= 64 on the tcgen05
+// gemv_w4_umma.cu -- W4A16 linear layer for 9 <= M <= 64 on the tcgen05
 // tensor core (sm_103a).
 //
 //   out[M,N] = x[M,K] . dequant(Wq)[N,K]^T,   dequant(q) = (q - z) * s
@@ -68,10 +68,14 @@ constexpr int UT_FIRST_EPI = 2;
 constexpr int UT_FIRST_DQ = UT_FIRST_EPI + UT_EPI_WARPS;
 constexpr int UT_MMA1 = UT_FIRST_DQ + UT_DQ_WARPS;             // MMA issuer of group 1
 constexpr int UT_THREADS = (UT_MMA1 + 1) * 32;
-constexpr int UT_NA = 4;             // A slots (one 64-K sub-block of both groups each)
+#ifndef W4Q_UMMA_NDB
+#define W4Q_UMMA_NDB 2
+#endif
+constexpr int UT_NDB = W4Q_UMMA_NDB;  // accumulator buffers (pairs in flight)
 constexpr uint32_t UT_TMEM_COLS = 512;
 constexpr uint32_t UT_DCOL = 128;    // columns per accumulator buffer (2 groups x NP <= 128)
-constexpr uint32_t UT_ACOL = 256;    // first A column (after two accumulator buffers)
+constexpr uint32_t UT_ACOL = UT_DCOL * UT_NDB;              // first A column
+constexpr int UT_NA = (int)((UT_TMEM_COLS - UT_ACOL) / 64);  // A slots (64-K sub-block, both groups)
 constexpr int UT_SMEM_LIMIT = 227 * 1024;
 
 struct UParams {
@@ -265,15 +269,15 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             for (int i = 0; i < n_iter && ok; ++i) {
                 const int slot = i % S;
                 if (!mbar_wait_sleep(full0 + 8 * slot, (uint32_t)(i / S) & 1u) ||
-                    (first && !mbar_wait_sleep(dempty0 + 8 * (d_it & 1),
-                                                 (uint32_t)((d_it >> 1) & 1) ^ 1u))) {
+                    (first && !mbar_wait_sleep(dempty0 + 8 * (d_it % UT_NDB),
+                                                 (uint32_t)((d_it / UT_NDB) & 1) ^ 1u))) {
                     report_error(p.err, ERR_FULL_WAIT);
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const bool live = gi == 0 || 2 * gp + 1 < p.G;
-                const uint32_t d_tmem = tmem + UT_DCOL * (uint32_t)(d_it & 1) + (uint32_t)(gi * NP);
+                const uint32_t d_tmem = tmem + UT_DCOL * (uint32_t)(d_it % UT_NDB) + (uint32_t)(gi * NP);
                 const uint64_t bdesc = sdesc_sw128_kmajor(smem_addr(smem + slot * SB));
                 for (int sbk = 0; sbk < 4; ++sbk) {
                     const int k = a_it % UT_NA;
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                 umma_commit(empty0 + 8 * slot);
                 first = false;
                 if (++b == p.KB || i == n_iter - 1) {  // the pair's last unit in this range
-                    umma_commit(dfull0 + 8 * (d_it & 1));
+                    umma_commit(dfull0 + 8 * (d_it % UT_NDB));
                     ++d_it;
                     first = true;
                     b = 0;
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
         const size_t seg = (size_t)p.M * UT_PAIR_ROWS;
         const int gp_last = n_iter > 0 ? (int)((u1 - 1) / p.KB) : gp_first - 1;
         for (int gp = gp_first, d = 0; gp <= gp_last; ++gp, ++d) {
-            if (!mbar_wait_sleep(dfull0 + 8 * (d & 1), (uint32_t)(d >> 1) & 1u)) {
+            if (!mbar_wait_sleep(dfull0 + 8 * (d % UT_NDB), (uint32_t)(d / UT_NDB) & 1u)) {
                 report_error(p.err, ERR_FULL_WAIT);
                 break;
             }
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
 #pragma unroll
                     for (int ch = 0; ch < CC / 8; ++ch)
                         tmem_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) +
-                                              UT_DCOL * (uint32_t)(d & 1) +
+                                              UT_DCOL * (uint32_t)(d % UT_NDB) +
                                               (uint32_t)(gi * NP + c0 + 8 * ch),
                                           r[ch]);
                     tmem_wait_ld();
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(dempty0 + 8 * (d & 1));
+                mbar_arrive(dempty0 + 8 * (d % UT_NDB));
         }
     } else {
         // ---------------------------------------------------------- dequant

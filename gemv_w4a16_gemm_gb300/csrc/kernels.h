@@ -25,10 +25,10 @@ struct W4Plan {
     int P;          // CTAs
     int split;      // 0 = balanced (stream-K) ranges, s >= 1 = fixed split
     int NB;         // n8 blocks of the MMA: 1, 2, 4 or 8
-    bool fold;      // dequantized weight rounded to bf16 (q - z) * s
+    bool fold;      // dequantized weight rounded to bf16 (q - z) * s (the umma path)
     bool fixup;     // some tile group is split over CTAs
     size_t partial_bytes;  // fp32 partials [P][2][M][128] ([P][2][M][256] for umma)
-    bool umma;      // tcgen05 kernel (W4A16, M > 16): units are pairs of tile groups
+    bool umma;      // tcgen05 kernel (W4A16, M >= 9): units are pairs of tile groups
     int NP;         // umma: M rounded up to 16 (the MMA's N)
     int G2;         // umma: ceil(G / 2) pairs of tile groups
 };
@@ -46,7 +46,7 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
                       void *out, int32_t *dots, void *workspace, unsigned *err,
                       cudaStream_t stream);
 
-// --- W4A16 on the tcgen05 tensor core, 16 < M <= 64 (gemv_w4_umma.cu)
+// --- W4A16 on the tcgen05 tensor core, 9 <= M <= 64 (gemv_w4_umma.cu)
 size_t w4_umma_workspace(const W4Plan &plan);
 size_t w4_umma_partial_bytes(int P, int M);
 cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed, void *out,

@@ -137,7 +137,7 @@ int w4_split_choice(int64_t M, int64_t N, int64_t K, int group);
  * with these sizes launches on the current device: the activation
  * preparation (W4A8 quantizer / W4A16 power-of-two prescale or tensor-core
  * operand layout, split-K counter reset) and the main kernel; for W4A16 at
- * M > 16 with row groups split over several CTAs, also the launch that sums
+ * M >= 9 with row groups split over several CTAs, also the launch that sums
  * their fp32 partials.  -1 when the sizes are unsupported. */
 int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
 
@@ -147,9 +147,10 @@ int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
  *   out        device, bf16 [M,N] row-major (written)
  *   workspace  device scratch of >= w4_workspace_bytes(M,N,K,group) bytes
  *              (may be NULL when that is 0); contents are clobbered.
- * Accumulates in fp32: per group, sum_k (q - z) * x exactly in the tensor
- * core, then acc += s * sum; for M > 16 the dequantized weight is rounded
- * once to bf16 ((q - z) * s) and accumulated over all of K.
+ * Accumulates in fp32: for M <= 8 per group, sum_k (q - z) * x exactly in
+ * the tensor core, then acc += s * sum; for M >= 9 the dequantized weight
+ * is rounded once to bf16 ((q - z) * s) and accumulated over all of K on
+ * the tcgen05 tensor core.
  * out = bf16_RN(acc).  Defined by "test_int4_quantized_gemm.py", the
  * dequant + F.linear reference. */
 int w4a16_gemm(const void *x_bf16, const void *packed, void *out_bf16,
