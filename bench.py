@@ -47,14 +47,11 @@ WORKLOAD = "decode_linear_suite"
 # the roofline reports traffic as null.
 MEASURED_TRAFFIC = {
     "w4a16 N=39936 K=6656 M=64": (
-        164434432, ("gemv_w4.cu", "common.cuh"),
-        "8474da36d5a74f37a8d1966eafac78c2fd2d6035549783d61252dca74fc7e7b5"),
+        164495616, ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh"),
+        "ba9e43b3fee10a1e76f5c6d276feb95408179bdea1fe784e5c7c7a1af5b08620"),
     "w4a16 N=39936 K=6656 M=4": (
-        161038848, ("gemv_w4.cu", "common.cuh"),
-        "8474da36d5a74f37a8d1966eafac78c2fd2d6035549783d61252dca74fc7e7b5"),
-    "w8 N=8192 K=8192 M=1": (
-        67288576, ("w8.cu", "common.cuh"),
-        "da7b7de323a6abb51a65ed52e37a552be8e2acea241096c0cb5610fca719ef7a"),
+        161016320, ("gemv_w4.cu", "common.cuh"),
+        "f748e2e1c9065f0c43ad3d44bb7beb75c393f28adee8c779e450e6f66fcd90b9"),
 }
 
 
