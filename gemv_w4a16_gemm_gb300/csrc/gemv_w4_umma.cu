@@ -36,6 +36,14 @@
 // kernel would leave M x (contributors) dependent L2 round trips per thread
 // at the tail of the kernel.
 //
+// Bounds (derived for every launch the plan can make): packed sources stay
+// below ceil(N/128) * 8 * KB * 2432 bytes (group 2gp + 1 of a pair is
+// copied only when 2gp + 1 < G); activation sources below KB * NP * 512;
+// shared-memory stages inside S * stage bytes of a 1024-aligned base; TMEM
+// columns below 512 (accumulators [0, 256), A slots 256 + 64k + 32g + 8j
+// + 8 <= 512); partial indices below P * 2 * M * 256; outputs only for
+// n < N and m < M.
+//
 // Pipelines (every wait sleeps in mbarrier.try_wait and gives up after one
 // second of %globaltimer):
 //   producer --full[s]--> dequant + MMA      (packed codes and x of stage s)
