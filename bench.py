@@ -402,7 +402,7 @@ def run_gpu(args, rank, world, dist):
                 "kernel": dom["kernel"], "call": dom["call"],
                 "algorithmic_bytes_per_launch": dom_alg, "us_per_launch": round(dom["us"], 3),
                 "peak_source": peaks["source"]}
-    value = world * step_weight / (ms * 1e-3) / 1e9
+    value = replica_value(world, step_weight, ms)
     w8 = next(c for c in per_call if c["kind"] == "w8")
     clocks = clk.summary()
     line = {
@@ -436,6 +436,12 @@ def run_gpu(args, rank, world, dist):
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+def replica_value(world, step_bytes, ms_max):
+    """Whole-job GB/s of `world` replicas that each stream `step_bytes` per
+    step, timed by the slowest rank (`ms_max`, milliseconds per step)."""
+    return world * step_bytes / (ms_max * 1e-3) / 1e9
 
 
 def _max_over_ranks(v, dist):
