@@ -117,7 +117,8 @@ __host__ __device__ constexpr int stages_for()
 template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int smem_for()
 {
-    return stages_for<NB, MODE>() * stage_bytes<NB, MODE>() + 2 * stages_for<NB, MODE>() * 8;
+    // + barriers + a 16-byte zero row (the B rows of the column-packed stage that are zero)
+    return stages_for<NB, MODE>() * stage_bytes<NB, MODE>() + 2 * stages_for<NB, MODE>() * 8 + 16;
 }
 
 // One stage: this warp's 16 x 256 tile, 4 sub-blocks of 64 K (two groups
@@ -224,7 +225,111 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
     }
 }
 
-template <int NB, W4Mode MODE>
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// One stage at NB = 1 with MP = 1, 2 or 4 rows of x per accumulator slot:
+// the 8 columns of the m16n8k16 accumulator hold 8 / MP groups x MP rows
+// (column n: group slot n / MP, row n % MP).  For the MMAs of a group, the
+// B columns of the other slots are zero: ldmatrix takes each row's address
+// per lane, so those lanes point at a 16-byte zero row (zaddr) and the others
+// at the x' row of their column.  One accumulator thus sums the dots of
+// 8 / MP groups side by side, and the fp32 scale / zero update runs once per
+// 8 / MP groups instead of once per group.  The lanes of one accumulator row
+// hold different slots of the same outputs; the flush adds them.
+template <int MP, bool DOTS>
+__device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xbase,
+                                                     uint32_t sbase, uint32_t zaddr, int lane,
+                                                     float (&acc)[1][4], const Params &p, int tile,
+                                                     int b)
+{
+    constexpr int GP = 8 / MP;  // groups per accumulator round
+    const int r = lane >> 2, c2 = 2 * (lane & 3);
+    // ldmatrix.x4 row of this lane: matrix q = (step +q>>1, k half q&1), B column n
+    const int bn = lane & 7, q = lane >> 3, bslot = bn / MP;
+    const uint32_t brow = xbase + (bn % MP) * XROW + 32 * (q >> 1) + 16 * (q & 1);
+    const int s0 = c2 / MP, s1 = (c2 + 1) / MP, m0 = c2 % MP, m1 = (c2 + 1) % MP;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t wv[16];  // word of step st: codes of rows r, r + 8 (step = 2 * group + half)
+#pragma unroll
+    for (int sbk = 0; sbk < 4; ++sbk) {
+        const uint4 wq = lds128(wbase + 512 * sbk + 16 * lane);
+        wv[4 * sbk] = wq.x;
+        wv[4 * sbk + 1] = wq.y;
+        wv[4 * sbk + 2] = wq.z;
+        wv[4 * sbk + 3] = wq.w;
+    }
+    // A round's groups go to NACC accumulators (short MMA dependency chains);
+    // their columns are disjoint, so adding them afterwards is exact.
+    constexpr int NACC = GP >= 4 ? 4 : GP, GPA = GP / NACC;
+#pragma unroll
+    for (int R = 0; R < MP; ++R) {
+        float dacc[NACC][4];
+#pragma unroll
+        for (int pp = 0; pp < GP; ++pp) {  // group R * GP + pp: steps 2g, 2g + 1
+            const int g = R * GP + pp, ai = pp / GPA;
+            uint32_t bf[2][2];
+            ldmatrix_x4(bslot == pp ? brow + 64 * g : zaddr, bf[0][0], bf[0][1], bf[1][0], bf[1][1]);
+#pragma unroll
+            for (int st = 0; st < 2; ++st) {
+                const uint32_t w = wv[2 * g + st], t = w >> 8;
+                uint32_t a[4];  // q * 2^-133 (low nibbles), q * 2^-129 (high nibbles)
+                a[0] = w & 0x000F000Fu;
+                a[1] = t & 0x000F000Fu;
+                a[2] = w & 0x00F000F0u;
+                a[3] = t & 0x00F000F0u;
+                if (pp % GPA == 0 && st == 0)
+                    mma_bf16(dacc[ai], a, bf[st][0], bf[st][1], zero4);
+                else
+                    mma_bf16(dacc[ai], a, bf[st][0], bf[st][1], dacc[ai]);
+            }
+        }
+        float d[4] = {dacc[0][0], dacc[0][1], dacc[0][2], dacc[0][3]};
+#pragma unroll
+        for (int ai = 1; ai < NACC; ++ai)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                d[e] += dacc[ai][e];
+        // the groups of this lane's two columns in this round
+        const int g0 = R * GP + s0, g1 = R * GP + s1;
+        const uint32_t sp0 = lds32(wbase + 2048 + ((g0 & 4) ? 128 : 0) + 16 * r + 4 * (g0 & 3));
+        const uint32_t zw0 = lds32(wbase + 2304 + 16 * r + 4 * (g0 >> 1));
+        const uint32_t sp1 = MP == 1 ? lds32(wbase + 2048 + ((g1 & 4) ? 128 : 0) + 16 * r + 4 * (g1 & 3)) : sp0;
+        const uint32_t zw1 = MP == 1 ? lds32(wbase + 2304 + 16 * r + 4 * (g1 >> 1)) : zw0;
+        const float xs0 = __uint_as_float(lds32(sbase + m0 * SROW + 4 * g0));
+        const float xs1 = __uint_as_float(lds32(sbase + m1 * SROW + 4 * g1));
+        const uint32_t zb0 = (uint32_t)((2 * g0) & 3), zb1 = (uint32_t)((2 * g1) & 3);
+        // -z as fp32: bytes [z, 0, 0, 0x4B] = 2^23 + z
+        const float nz0 = 8388608.0f - __uint_as_float(prmt(zw0, 0x4B000000u, 0x7440u + zb0));
+        const float nz08 = 8388608.0f - __uint_as_float(prmt(zw0, 0x4B000000u, 0x7440u + zb0 + 1));
+        const float nz1 = MP == 1 ? 8388608.0f - __uint_as_float(prmt(zw1, 0x4B000000u, 0x7440u + zb1)) : nz0;
+        const float nz18 =
+            MP == 1 ? 8388608.0f - __uint_as_float(prmt(zw1, 0x4B000000u, 0x7440u + zb1 + 1)) : nz08;
+        if (DOTS) {
+            const int G = p.K / 32;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = (e & 1) ? m1 : m0, g = (e & 1) ? g1 : g0;
+                const int n = tile * 16 + r + 8 * (e >> 1);
+                const float nz = (e & 1) ? ((e >> 1) ? nz18 : nz1) : ((e >> 1) ? nz08 : nz0);
+                const float dg = fmaf(nz, (e & 1) ? xs1 : xs0, d[e]);
+                if (m < p.M && n < p.N)
+                    p.dots[((size_t)m * p.N + n) * G + b * 8 + g] = (int32_t)rintf(dg * 4096.0f);
+            }
+        } else {
+            acc[0][0] = fmaf(bf16lo_to_f32(sp0), fmaf(nz0, xs0, d[0]), acc[0][0]);
+            acc[0][1] = fmaf(bf16lo_to_f32(sp1), fmaf(nz1, xs1, d[1]), acc[0][1]);
+            acc[0][2] = fmaf(bf16hi_to_f32(sp0), fmaf(nz08, xs0, d[2]), acc[0][2]);
+            acc[0][3] = fmaf(bf16hi_to_f32(sp1), fmaf(nz18, xs1, d[3]), acc[0][3]);
+        }
+    }
+}
+
+template <int NB, W4Mode MODE, int MP>
 __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Params p)
 {
     constexpr bool DOTS = MODE == W4Mode::A8_DOTS;
@@ -236,6 +341,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * SB);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + STAGES);
+    const uint32_t zrow = smem_addr(bars + 2 * STAGES);  // 16 zero bytes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -247,6 +353,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, WARPS);
         }
+        *reinterpret_cast<uint4 *>(bars + 2 * STAGES) = make_uint4(0u, 0u, 0u, 0u);
         fence_barrier_init();
     }
     {   // activation rows m >= M of every stage stay zero (never copied into)
@@ -356,6 +463,19 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
         auto flush = [&](int g) {
             if (DOTS)
                 return;
+            if constexpr (NB == 1 && MP < 8) {
+                // add the slots: lanes of one row hold other groups of the same outputs
+                if (MP == 1) {
+                    acc[0][0] += acc[0][1];
+                    acc[0][2] += acc[0][3];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (MP <= 2)
+                        acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], 1);
+                    acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], 2);
+                }
+            }
             const int tile = g * WARPS + warp;
             if (tile >= p.T)
                 return;
@@ -438,10 +558,18 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             }
             const int tile = g * WARPS + warp;
             if (tile < p.T)
-                compute_stage<NB, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
-                                              smem_addr(smem + slot * SB + XOFF),
-                                              smem_addr(smem + slot * SB + SOFF), lane, acc, p,
-                                              tile, b);
+            {
+                if constexpr (NB == 1 && MP < 8)
+                    compute_stage_packed<MP, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
+                                                   smem_addr(smem + slot * SB + XOFF),
+                                                   smem_addr(smem + slot * SB + SOFF), zrow, lane,
+                                                   acc, p, tile, b);
+                else
+                    compute_stage<NB, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
+                                            smem_addr(smem + slot * SB + XOFF),
+                                            smem_addr(smem + slot * SB + SOFF), lane, acc, p,
+                                            tile, b);
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * slot);
@@ -623,7 +751,7 @@ int ctas_per_sm(int dev)
     if (dev < 0 || dev >= 64)
         return 1;
     if (cache[dev] == 0) {
-        auto fn = w4_kernel<NB, MODE>;
+        auto fn = w4_kernel<NB, MODE, 8>;  // occupancy is set by shared memory, not MP
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_for<NB, MODE>());
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, THREADS, smem_for<NB, MODE>()) !=
@@ -637,6 +765,16 @@ int ctas_per_sm(int dev)
 
 int nb_for(int M) { return M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8)); }
 
+// Rows of x per accumulator slot at NB = 1 (M rounded up to a power of two).
+#ifndef W4Q_MP_MIN
+#define W4Q_MP_MIN 1
+#endif
+int mp_for(int M)
+{
+    const int mp = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+    return mp < W4Q_MP_MIN ? W4Q_MP_MIN : mp;
+}
+
 template <W4Mode MODE>
 int ctas_per_sm_for(int NB, int dev)
 {
@@ -648,10 +786,10 @@ int ctas_per_sm_for(int NB, int dev)
     }
 }
 
-template <int NB, W4Mode MODE>
+template <int NB, W4Mode MODE, int MP>
 cudaError_t launch_main(const Params &p, cudaStream_t stream)
 {
-    auto fn = w4_kernel<NB, MODE>;
+    auto fn = w4_kernel<NB, MODE, MP>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem_for<NB, MODE>());
     if (e != cudaSuccess)
@@ -672,11 +810,22 @@ cudaError_t launch_main(const Params &p, cudaStream_t stream)
 template <W4Mode MODE>
 cudaError_t dispatch_main(const W4Plan &plan, const Params &p, cudaStream_t stream)
 {
-    switch (plan.NB) {
-    case 1: return launch_main<1, MODE>(p, stream);
-    case 2: return launch_main<2, MODE>(p, stream);
-    case 4: return launch_main<4, MODE>(p, stream);
-    default: return launch_main<8, MODE>(p, stream);
+    if (plan.NB == 1) {
+        switch (mp_for(plan.M)) {
+        case 1: return launch_main<1, MODE, 1>(p, stream);
+        case 2: return launch_main<1, MODE, 2>(p, stream);
+        case 4: return launch_main<1, MODE, 4>(p, stream);
+        default: return launch_main<1, MODE, 8>(p, stream);
+        }
+    }
+    if constexpr (MODE == W4Mode::A16) {
+        return cudaErrorInvalidValue;  // W4A16 above 8 rows runs on the tcgen05 kernel
+    } else {
+        switch (plan.NB) {
+        case 2: return launch_main<2, MODE, 8>(p, stream);
+        case 4: return launch_main<4, MODE, 8>(p, stream);
+        default: return launch_main<8, MODE, 8>(p, stream);
+        }
     }
 }
 
@@ -743,7 +892,7 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
         int dev = 0;
         cudaGetDevice(&dev);
         const int per_sm = pl.umma ? 1
-                           : (mode == W4Mode::A16) ? ctas_per_sm_for<W4Mode::A16>(pl.NB, dev)
+                           : (mode == W4Mode::A16) ? ctas_per_sm<1, W4Mode::A16>(dev)
                                                    : ctas_per_sm_for<W4Mode::A8>(pl.NB, dev);
         const long long slots = (long long)(sm_count > 0 ? sm_count : 1) * per_sm;
         pl.split = 0;
