@@ -48,10 +48,10 @@ WORKLOAD = "decode_linear_suite"
 MEASURED_TRAFFIC = {
     "w4a16 N=39936 K=6656 M=64": (
         164495616, ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh"),
-        "ba9e43b3fee10a1e76f5c6d276feb95408179bdea1fe784e5c7c7a1af5b08620"),
+        "d62926a3187e98307c2913bae7b652b284f8fdd32da19bb5fbc037406ab7fbbf"),
     "w4a16 N=39936 K=6656 M=4": (
-        161016320, ("gemv_w4.cu", "common.cuh"),
-        "f748e2e1c9065f0c43ad3d44bb7beb75c393f28adee8c779e450e6f66fcd90b9"),
+        161181440, ("gemv_w4.cu", "common.cuh"),
+        "8cbca7a8a80cf0b433f9304d390324387197f699584d1e23ada76f2ee2ee550a"),
 }
 
 
