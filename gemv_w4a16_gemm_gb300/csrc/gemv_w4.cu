@@ -72,6 +72,7 @@ struct Params {
     const uint8_t *packed;
     const __nv_bfloat16 *x;  // bf16 [K/256][M][264]: x' (prepared)
     const float *xsum;       // fp32 [K/256][M][8]: X'
+    const float *gscale;     // fp32 [K/256][M][8]: W4A8 activation scale x 2^12 per group
     const float *oscale;     // fp32 [M]: output scale per row
     __nv_bfloat16 *out;      // bf16 [M][N]
     int32_t *dots;           // group-dot export: int32 [M][N][K/32]
@@ -102,7 +103,8 @@ __device__ __forceinline__ int range_owner(const Params &p, long long u)
 template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int stage_bytes()
 {
-    return WARPS * TILE_BYTES + NB * 8 * XROW + NB * 8 * SROW;
+    // codes, x' rows, X' rows, and for W4A8 the per-group activation scales
+    return WARPS * TILE_BYTES + NB * 8 * XROW + NB * 8 * SROW * (MODE == W4Mode::A8 ? 2 : 1);
 }
 
 template <int NB, W4Mode MODE>
@@ -121,13 +123,20 @@ __host__ __device__ constexpr int smem_for()
     return stages_for<NB, MODE>() * stage_bytes<NB, MODE>() + 2 * stages_for<NB, MODE>() * 8 + 16;
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 // One stage: this warp's 16 x 256 tile, 4 sub-blocks of 64 K (two groups
 // each), 4 k16 steps per sub-block.  xbase: the stage's activation rows;
 // sbase: the stage's group sums.
-template <int NB, bool DOTS>
+template <int NB, bool DOTS, bool GS>
 __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, uint32_t sbase,
-                                              int lane, float (&acc)[NB][4], const Params &p,
-                                              int tile, int b)
+                                              uint32_t gbase, int lane, float (&acc)[NB][4],
+                                              const Params &p, int tile, int b)
 {
     const int r = lane >> 2, c2 = 2 * (lane & 3);
     const uint4 sc0 = lds128(wbase + 2048 + 16 * r);
@@ -214,10 +223,13 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
                     const float sr = bf16lo_to_f32(sp), sr8 = bf16hi_to_f32(sp);
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
-                        acc[nb][0] = fmaf(sr, fmaf(nzr, xs[nb][0][g], d[nb][0]), acc[nb][0]);
-                        acc[nb][1] = fmaf(sr, fmaf(nzr, xs[nb][1][g], d[nb][1]), acc[nb][1]);
-                        acc[nb][2] = fmaf(sr8, fmaf(nzr8, xs[nb][0][g], d[nb][2]), acc[nb][2]);
-                        acc[nb][3] = fmaf(sr8, fmaf(nzr8, xs[nb][1][g], d[nb][3]), acc[nb][3]);
+                        // W4A8: times the activation scale of (column, group)
+                        const float g0 = GS ? __uint_as_float(lds32(gbase + (nb * 8 + c2) * SROW + 4 * g)) : 1.f;
+                        const float g1 = GS ? __uint_as_float(lds32(gbase + (nb * 8 + c2 + 1) * SROW + 4 * g)) : 1.f;
+                        acc[nb][0] = fmaf(GS ? sr * g0 : sr, fmaf(nzr, xs[nb][0][g], d[nb][0]), acc[nb][0]);
+                        acc[nb][1] = fmaf(GS ? sr * g1 : sr, fmaf(nzr, xs[nb][1][g], d[nb][1]), acc[nb][1]);
+                        acc[nb][2] = fmaf(GS ? sr8 * g0 : sr8, fmaf(nzr8, xs[nb][0][g], d[nb][2]), acc[nb][2]);
+                        acc[nb][3] = fmaf(GS ? sr8 * g1 : sr8, fmaf(nzr8, xs[nb][1][g], d[nb][3]), acc[nb][3]);
                     }
                 }
             }
@@ -225,12 +237,6 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
     }
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
 
 // One stage at NB = 1 with MP = 1, 2 or 4 rows of x per accumulator slot:
 // the 8 columns of the m16n8k16 accumulator hold 8 / MP groups x MP rows
@@ -241,11 +247,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 // 8 / MP groups side by side, and the fp32 scale / zero update runs once per
 // 8 / MP groups instead of once per group.  The lanes of one accumulator row
 // hold different slots of the same outputs; the flush adds them.
-template <int MP, bool DOTS>
+template <int MP, bool DOTS, bool GS>
 __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xbase,
-                                                     uint32_t sbase, uint32_t zaddr, int lane,
-                                                     float (&acc)[1][4], const Params &p, int tile,
-                                                     int b)
+                                                     uint32_t sbase, uint32_t gbase, uint32_t zaddr,
+                                                     int lane, float (&acc)[1][4], const Params &p,
+                                                     int tile, int b)
 {
     constexpr int GP = 8 / MP;  // groups per accumulator round
     const int r = lane >> 2, c2 = 2 * (lane & 3);
@@ -321,10 +327,13 @@ __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xb
                     p.dots[((size_t)m * p.N + n) * G + b * 8 + g] = (int32_t)rintf(dg * 4096.0f);
             }
         } else {
-            acc[0][0] = fmaf(bf16lo_to_f32(sp0), fmaf(nz0, xs0, d[0]), acc[0][0]);
-            acc[0][1] = fmaf(bf16lo_to_f32(sp1), fmaf(nz1, xs1, d[1]), acc[0][1]);
-            acc[0][2] = fmaf(bf16hi_to_f32(sp0), fmaf(nz08, xs0, d[2]), acc[0][2]);
-            acc[0][3] = fmaf(bf16hi_to_f32(sp1), fmaf(nz18, xs1, d[3]), acc[0][3]);
+            // W4A8: times the activation scale of (row of x, group)
+            const float ga = GS ? __uint_as_float(lds32(gbase + m0 * SROW + 4 * g0)) : 1.f;
+            const float gb = GS ? __uint_as_float(lds32(gbase + m1 * SROW + 4 * g1)) : 1.f;
+            acc[0][0] = fmaf(bf16lo_to_f32(sp0) * ga, fmaf(nz0, xs0, d[0]), acc[0][0]);
+            acc[0][1] = fmaf(bf16lo_to_f32(sp1) * gb, fmaf(nz1, xs1, d[1]), acc[0][1]);
+            acc[0][2] = fmaf(bf16hi_to_f32(sp0) * ga, fmaf(nz08, xs0, d[2]), acc[0][2]);
+            acc[0][3] = fmaf(bf16hi_to_f32(sp1) * gb, fmaf(nz18, xs1, d[3]), acc[0][3]);
         }
     }
 }
@@ -337,6 +346,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     constexpr int SB = stage_bytes<NB, MODE>();
     constexpr int XOFF = WARPS * TILE_BYTES;     // activation rows within a stage
     constexpr int SOFF = XOFF + NB * 8 * XROW;   // group sums within a stage
+    constexpr int GOFF = SOFF + NB * 8 * SROW;   // W4A8 group scales within a stage
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * SB);
@@ -358,13 +368,17 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     }
     {   // activation rows m >= M of every stage stay zero (never copied into)
         const int pad_rows = NB * 8 - p.M;
-        const int xper = pad_rows * (XROW / 16), sper = pad_rows * (SROW / 16);
+        const int xper = pad_rows * (XROW / 16);
+        const int sper = pad_rows * (SROW / 16) * (MODE == W4Mode::A8 ? 2 : 1);
         for (int i = threadIdx.x; i < STAGES * (xper + sper); i += THREADS) {
             const int s = i / (xper + sper), rem = i % (xper + sper);
             uint8_t *dst = rem < xper
                                ? smem + s * SB + XOFF + (p.M + rem / (XROW / 16)) * XROW +
                                      (rem % (XROW / 16)) * 16
-                               : smem + s * SB + SOFF + (p.M + (rem - xper) / 2) * SROW +
+                               : (rem - xper < pad_rows * 2
+                                      ? smem + s * SB + SOFF + (p.M + (rem - xper) / 2) * SROW
+                                      : smem + s * SB + GOFF +
+                                            (p.M + (rem - xper - pad_rows * 2) / 2) * SROW) +
                                      ((rem - xper) % 2) * 16;
             *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -380,7 +394,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             const uint32_t xbytes = (uint32_t)p.M * XROW, sbytes = (uint32_t)p.M * SROW;
-            const uint32_t act_bytes = xbytes + sbytes;
+            const uint32_t act_bytes = xbytes + sbytes * (MODE == W4Mode::A8 ? 2u : 1u);
             auto issue_w = [&](int i, int g, int b) {
                 const int slot = i % STAGES;
                 const uint32_t bar = full0 + 8 * slot;
@@ -396,6 +410,9 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                          p.x + (size_t)b * p.M * (XROW / 2), xbytes, bar, pol_x);
                 bulk_g2s(smem_addr(smem + slot * SB + SOFF),
                          p.xsum + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
+                if (MODE == W4Mode::A8)
+                    bulk_g2s(smem_addr(smem + slot * SB + GOFF),
+                             p.gscale + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
             };
             // Prologue: two stages of weights go out at once; the activation
             // copies follow as soon as act_prep has finished.  The other
@@ -560,15 +577,15 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             if (tile < p.T)
             {
                 if constexpr (NB == 1 && MP < 8)
-                    compute_stage_packed<MP, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
-                                                   smem_addr(smem + slot * SB + XOFF),
-                                                   smem_addr(smem + slot * SB + SOFF), zrow, lane,
-                                                   acc, p, tile, b);
+                    compute_stage_packed<MP, DOTS, MODE == W4Mode::A8>(
+                        smem_addr(smem + slot * SB + warp * TILE_BYTES),
+                        smem_addr(smem + slot * SB + XOFF), smem_addr(smem + slot * SB + SOFF),
+                        smem_addr(smem + slot * SB + GOFF), zrow, lane, acc, p, tile, b);
                 else
-                    compute_stage<NB, DOTS>(smem_addr(smem + slot * SB + warp * TILE_BYTES),
-                                            smem_addr(smem + slot * SB + XOFF),
-                                            smem_addr(smem + slot * SB + SOFF), lane, acc, p,
-                                            tile, b);
+                    compute_stage<NB, DOTS, MODE == W4Mode::A8>(
+                        smem_addr(smem + slot * SB + warp * TILE_BYTES),
+                        smem_addr(smem + slot * SB + XOFF), smem_addr(smem + slot * SB + SOFF),
+                        smem_addr(smem + slot * SB + GOFF), lane, acc, p, tile, b);
             }
             __syncwarp();
             if (lane == 0)
@@ -611,8 +628,8 @@ constexpr int PREP_CHUNK = PREP_THREADS * 8;  // columns one CTA transforms
 template <int KIND>
 __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     const __nv_bfloat16 *__restrict__ x, int M, int K, __nv_bfloat16 *__restrict__ xp,
-    float *__restrict__ xsum, float *__restrict__ oscale, unsigned *__restrict__ counters,
-    int ncounters)
+    float *__restrict__ xsum, float *__restrict__ gscale, float *__restrict__ oscale,
+    unsigned *__restrict__ counters, int ncounters)
 {
     pdl_launch_dependents();  // the main kernel may start streaming weights
     pdl_wait();               // x (and this workspace) may belong to the previous kernel
@@ -620,60 +637,75 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     const int bid = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = bid * PREP_THREADS + threadIdx.x; i < ncounters; i += nblk * PREP_THREADS)
         counters[i] = 0u;
-    __shared__ float red[PREP_THREADS / 32];
     const int m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
     const int n8 = K / 8;
-    float a = 0.f;
-    for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
-        const uint4 v = row[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int sigma = 121;  // x' = value * 2^sigma on lower half-steps (2^(sigma-4) upper)
+    if (KIND == PREP_A16) {
+        // the power-of-two prescale from the row's max |x|
+        __shared__ float red[PREP_THREADS / 32];
+        float a = 0.f;
+        for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
+            const uint4 v = row[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
-    }
+            for (int j = 0; j < 4; ++j)
+                a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = a;
-    __syncthreads();
-    a = 0.f;
+        for (int o = 16; o > 0; o >>= 1)
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if ((threadIdx.x & 31) == 0)
+            red[threadIdx.x >> 5] = a;
+        __syncthreads();
+        a = 0.f;
 #pragma unroll
-    for (int i = 0; i < PREP_THREADS / 32; ++i)
-        a = fmaxf(a, red[i]);
-    float sxm = 0.f;  // W4A8 activation scale
-    int sigma = 0;    // x' = value * 2^sigma on lower half-steps (2^(sigma-4) upper)
-    if (KIND == PREP_A8) {
-        sxm = __fdiv_rn(a, 127.0f);
-        sigma = 121;
-    } else {
+        for (int i = 0; i < PREP_THREADS / 32; ++i)
+            a = fmaxf(a, red[i]);
         int e = 0;
         if (a > 0.f)
             (void)frexpf(a, &e);  // a < 2^e
         sigma = min(max(128 - e, 6), 259);
     }
     if (threadIdx.x == 0 && blockIdx.y == 0)
-        oscale[m] = KIND == PREP_A8 ? sxm * 4096.0f : ldexpf(1.0f, 133 - sigma);
-    // 8 consecutive values per thread; 4 threads per group of 32
+        oscale[m] = KIND == PREP_A8 ? 1.0f : ldexpf(1.0f, 133 - sigma);
+    // 8 consecutive values per thread; 4 consecutive threads per group of 32
     const int i = blockIdx.y * PREP_THREADS + threadIdx.x;
     const bool live = i < n8;
-    float part = 0.f;
+    float v[8];
     if (live) {
-        const int k0 = 8 * i;
         const uint4 raw = row[i];
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float v[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             v[2 * j] = bf16lo_to_f32(w[j]);
             v[2 * j + 1] = bf16hi_to_f32(w[j]);
         }
-        if (KIND == PREP_A8) {
+    } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxm)), -127.f), 127.f);
+        for (int j = 0; j < 8; ++j)
+            v[j] = 0.f;
+    }
+    if (KIND == PREP_A8) {
+        // one scale per group of 32: sx = fp32(max |x| / 127), xq = clamp(rint(x / sx))
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            a = fmaxf(a, fabsf(v[j]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const float sxg = __fdiv_rn(a, 127.0f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxg)), -127.f), 127.f);
+        if (live && (i & 3) == 0) {
+            const int g = i / 4;  // x 2^12: the group dots come out of the MMA scaled by 2^-12
+            gscale[((size_t)(g / 8) * M + m) * 8 + (g % 8)] = sxg * 4096.0f;
         }
+    }
+    float part = 0.f;
+    if (live) {
+        const int k0 = 8 * i;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             part += v[j];
@@ -698,47 +730,48 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     }
 }
 
-// W4A8 activation quantizer alone (int8 output; the test view of the same
-// rule act_prep applies).
+// W4A8 activation quantizer alone (int8 output, one fp32 scale per (row,
+// group of 32); the test view of the same rule act_prep applies).  One CTA
+// per row; 4 consecutive threads per group.
 __global__ void __launch_bounds__(512) act_quant_i8_kernel(const __nv_bfloat16 *__restrict__ x,
                                                            int K, int8_t *__restrict__ xq,
                                                            float *__restrict__ sx)
 {
-    __shared__ float red[16];
     const int m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
     const int n8 = K / 8;
-    float a = 0.f;
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        const uint4 v = row[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int i0 = 0; i0 < n8; i0 += blockDim.x) {  // blockDim is a multiple of 32
+        const int i = i0 + threadIdx.x;
+        float f[8];
+        if (i < n8) {
+            const uint4 v = row[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
-    }
+            for (int j = 0; j < 8; ++j)
+                f[j] = (j & 1) ? bf16hi_to_f32(w[j / 2]) : bf16lo_to_f32(w[j / 2]);
+        } else {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = a;
-    __syncthreads();
-    a = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
-        a = fmaxf(a, red[i]);
-    const float s = __fdiv_rn(a, 127.0f);
-    if (threadIdx.x == 0)
-        sx[m] = s;
-    for (int i = threadIdx.x; i < n8; i += blockDim.x) {
-        const uint4 v = row[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t q[2] = {0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float f = (j & 1) ? bf16hi_to_f32(w[j / 2]) : bf16lo_to_f32(w[j / 2]);
-            const float qf = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(f, s)), -127.f), 127.f);
-            q[j / 4] |= (uint32_t)(uint8_t)(int8_t)qf << (8 * (j % 4));
+            for (int j = 0; j < 8; ++j)
+                f[j] = 0.f;
         }
-        reinterpret_cast<uint2 *>(xq + (size_t)m * K)[i] = make_uint2(q[0], q[1]);
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            a = fmaxf(a, fabsf(f[j]));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const float s = __fdiv_rn(a, 127.0f);
+        if (i < n8) {
+            if ((i & 3) == 0)
+                sx[(size_t)m * (K / 32) + i / 4] = s;
+            uint32_t q[2] = {0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float qf = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(f[j], s)), -127.f), 127.f);
+                q[j / 4] |= (uint32_t)(uint8_t)(int8_t)qf << (8 * (j % 4));
+            }
+            reinterpret_cast<uint2 *>(xq + (size_t)m * K)[i] = make_uint2(q[0], q[1]);
+        }
     }
 }
 
@@ -775,16 +808,6 @@ int mp_for(int M)
     return mp < W4Q_MP_MIN ? W4Q_MP_MIN : mp;
 }
 
-template <W4Mode MODE>
-int ctas_per_sm_for(int NB, int dev)
-{
-    switch (NB) {
-    case 1: return ctas_per_sm<1, MODE>(dev);
-    case 2: return ctas_per_sm<2, MODE>(dev);
-    case 4: return ctas_per_sm<4, MODE>(dev);
-    default: return ctas_per_sm<8, MODE>(dev);
-    }
-}
 
 template <int NB, W4Mode MODE, int MP>
 cudaError_t launch_main(const Params &p, cudaStream_t stream)
@@ -818,26 +841,20 @@ cudaError_t dispatch_main(const W4Plan &plan, const Params &p, cudaStream_t stre
         default: return launch_main<1, MODE, 8>(p, stream);
         }
     }
-    if constexpr (MODE == W4Mode::A16) {
-        return cudaErrorInvalidValue;  // W4A16 above 8 rows runs on the tcgen05 kernel
-    } else {
-        switch (plan.NB) {
-        case 2: return launch_main<2, MODE, 8>(p, stream);
-        case 4: return launch_main<4, MODE, 8>(p, stream);
-        default: return launch_main<8, MODE, 8>(p, stream);
-        }
-    }
+    // W4A16 above 8 rows runs on the tcgen05 kernel; W4A8 is planned up to 8 rows
+    return cudaErrorInvalidValue;
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Workspace layout: [x' bf16 (K/256)*M*264][X' f32 (K/256)*M*8][out scale f32 M]
+// Workspace layout: [x' bf16 (K/256)*M*264][X' f32 (K/256)*M*8]
+//                   [W4A8 group scales f32 (K/256)*M*8][out scale f32 M]
 //                   [counters u32 G*8][partials f32 P*2*M*128], 256-byte aligned.
 struct WsLayout {
-    size_t xp, xsum, oscale, counters, partial, total;
+    size_t xp, xsum, gscale, oscale, counters, partial, total;
 };
 
-WsLayout ws_layout(const W4Plan &pl)
+WsLayout ws_layout(const W4Plan &pl, W4Mode mode)
 {
     WsLayout L;
     size_t o = 0;
@@ -845,6 +862,8 @@ WsLayout ws_layout(const W4Plan &pl)
     o += align_up((size_t)pl.KB * pl.M * XROW, 256);
     L.xsum = o;
     o += align_up((size_t)pl.KB * pl.M * SROW, 256);
+    L.gscale = o;
+    o += mode == W4Mode::A8 ? align_up((size_t)pl.KB * pl.M * SROW, 256) : 0;
     L.oscale = o;
     o += align_up((size_t)pl.M * 4, 256);
     L.counters = o;
@@ -861,6 +880,8 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
 {
     if (M < 1 || M > 64 || N < 1 || K < 256 || K % 256 != 0)
         return false;
+    if (mode != W4Mode::A16 && M > 8)
+        return false;  // W4A8 serves decode rows (the pages' buckets are 1..4)
     W4Plan pl = {};
     pl.M = M;
     pl.N = N;
@@ -893,7 +914,7 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
         cudaGetDevice(&dev);
         const int per_sm = pl.umma ? 1
                            : (mode == W4Mode::A16) ? ctas_per_sm<1, W4Mode::A16>(dev)
-                                                   : ctas_per_sm_for<W4Mode::A8>(pl.NB, dev);
+                                                   : ctas_per_sm<1, W4Mode::A8>(dev);
         const long long slots = (long long)(sm_count > 0 ? sm_count : 1) * per_sm;
         pl.split = 0;
         pl.P = (int)(U < slots ? U : slots);
@@ -910,8 +931,7 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
 
 size_t w4_workspace_for(const W4Plan &plan, W4Mode mode)
 {
-    (void)mode;
-    return plan.umma ? w4_umma_workspace(plan) : ws_layout(plan).total;
+    return plan.umma ? w4_umma_workspace(plan) : ws_layout(plan, mode).total;
 }
 
 cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void *packed,
@@ -920,7 +940,7 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
 {
     if (plan.umma)
         return launch_w4_umma(plan, x, packed, out, workspace, err, stream);
-    const WsLayout L = ws_layout(plan);
+    const WsLayout L = ws_layout(plan, mode);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     Params p = {};
     p.packed = static_cast<const uint8_t *>(packed);
@@ -938,6 +958,7 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     p.U = (long long)plan.G * plan.KB;
     p.x = reinterpret_cast<const __nv_bfloat16 *>(ws + L.xp);
     p.xsum = reinterpret_cast<const float *>(ws + L.xsum);
+    p.gscale = reinterpret_cast<const float *>(ws + L.gscale);
     p.oscale = reinterpret_cast<const float *>(ws + L.oscale);
     p.counters = reinterpret_cast<unsigned *>(ws + L.counters);
     p.partial = reinterpret_cast<float *>(ws + L.partial);
@@ -959,7 +980,8 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     auto prep = mode == W4Mode::A16 ? act_prep_kernel<PREP_A16> : act_prep_kernel<PREP_A8>;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prep, xin, plan.M, plan.K, xp, xsum, osc, cnt,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prep, xin, plan.M, plan.K, xp, xsum,
+                                       reinterpret_cast<float *>(ws + L.gscale), osc, cnt,
                                        ncounters);
     if (e != cudaSuccess)
         return e;

@@ -198,7 +198,7 @@ def w4a8_gemm(x, packed, N, K, group=GROUP, split_k=None, out=None, workspace=No
 def w4a8_quantize_act(x: torch.Tensor, stream=None):
     M, K = x.shape
     xq = torch.empty(M, K, dtype=torch.int8, device=x.device)
-    sx = torch.empty(M, dtype=torch.float32, device=x.device)
+    sx = torch.empty(M, K // GROUP, dtype=torch.float32, device=x.device)
     _check("w4a8_quantize_act", lib().w4a8_quantize_act(
         _cuda(x, torch.bfloat16, "x"), M, K, xq.data_ptr(), sx.data_ptr(), _stream(stream)))
     return xq, sx

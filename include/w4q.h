@@ -9,9 +9,9 @@
  *          ("test_int4_quantized_gemm.py": _packed_with_dense with
  *          QuantConfig(bits=4, group_size=32, symmetric=False,
  *          method="min_max"); the dequant + F.linear reference.)
- *   W4A8   the same weights, activations quantized per row to symmetric
- *          int8 inside the call; each group's dot product is an exact
- *          integer, scaled in fp32.  ("test_int4_quantized_gemm.py": the
+ *   W4A8   the same weights, activations quantized to symmetric int8
+ *          inside the call with one scale per (row, group of 32); each
+ *          group's dot product is an exact integer, scaled in fp32.  ("test_int4_quantized_gemm.py": the
  *          W4A8 bucket kernels and Int4QuantizedGemmPrecisionTest.)
  *   W8     int8 weights with one bf16 scale per output row.
  *          ("gpt-fast issue #114": WeightOnlyInt8Linear.forward,
@@ -191,11 +191,16 @@ int w4a16_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
 int w4a16_gemm_noalloc(const void *x_bf16, const void *packed, void *out_bf16, int64_t M,
                        int64_t N, int64_t K, int group, void *stream);
 
-/* out = x . dequant(packed)^T, W4A8: per row m, sx = fp32(max|x| / 127),
- * xq = clamp(rint(x / sx), -127, 127) in IEEE fp32 (xq = 0 when max|x| = 0);
- * per group D = sum_k (q - z) * xq, an exact integer (|D| <= 60960);
- * acc = sum_g s_g * D_g in fp32; out = bf16_RN(sx * acc).
- * Arguments as w4a16_gemm; the workspace is required (it holds xq and sx). */
+/* out = x . dequant(packed)^T, W4A8: per row m and group g of 32 columns,
+ * sx[m,g] = fp32(max_{k in g} |x| / 127), xq = clamp(rint(x / sx[m,g]),
+ * -127, 127) in IEEE fp32 (xq = 0 when the group's max is 0); per group
+ * D = sum_k (q - z) * xq, an exact integer (|D| <= 60960);
+ * acc = sum_g sx[m,g] * s_g * D_g in fp32; out = bf16_RN(acc).  One scale
+ * per group keeps an outlier channel from flattening its row: the outlier
+ * case of Int4QuantizedGemmPrecisionTest ("test_int4_quantized_gemm.py")
+ * fails with one scale per row.
+ * Arguments as w4a16_gemm with 1 <= M <= 8 (the pages' W4A8 buckets are
+ * 1..4); the workspace is required (it holds the prepared activations). */
 int w4a8_gemm(const void *x_bf16, const void *packed, void *out_bf16,
               int64_t M, int64_t N, int64_t K, int group, void *workspace,
               size_t workspace_bytes, void *stream);
@@ -204,12 +209,12 @@ int w4a8_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
                     int64_t M, int64_t N, int64_t K, int group, int split_k,
                     void *workspace, size_t workspace_bytes, void *stream);
 
-/* The W4A8 activation quantizer alone (same device code as w4a8_gemm).
- *   xq  device, int8 [M,K] (written);  sx  device, f32 [M] (written). */
+/* The W4A8 activation quantizer alone (the rule w4a8_gemm applies).
+ *   xq  device, int8 [M,K] (written);  sx  device, f32 [M][K/32] (written). */
 int w4a8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq,
                       float *sx, void *stream);
 
-/* The exact W4A8 group dot products, for bit-exact checks.
+/* The exact W4A8 group dot products, for bit-exact checks (1 <= M <= 8).
  *   D          device, int32 [M][N][K/32] (written)
  *   workspace  device, >= w4_workspace_bytes(M,N,K,group) bytes
  * Uses the same activation quantizer and the same tensor-core group dot as

@@ -150,11 +150,12 @@ def w4a16(x_bf16, q, s, z, n0: int = 0, n1: int | None = None) -> np.ndarray:
 
 
 def act_quant(x_bf16, K: int):
-    """Per-row symmetric int8 activations: (xq i8 [M,K], sx f32 [M])."""
+    """Symmetric int8 activations, one scale per (row, group of 32):
+    (xq i8 [M,K], sx f32 [M, K/32])."""
     x = _u16(x_bf16).reshape(-1, K)
     M = x.shape[0]
     xq = np.empty((M, K), np.int8)
-    sx = np.empty(M, np.float32)
+    sx = np.empty((M, K // GROUP), np.float32)
     _load().oracle_act_quant(_ptr(x), M, K, _ptr(xq), _ptr(sx))
     return xq, sx
 

@@ -294,41 +294,46 @@ void oracle_w4a16(const uint16_t *x, const uint8_t *q, const uint16_t *s,
 }
 
 /* ------------------------------------------------------------------ */
-/* W4A8: per-row symmetric int8 activations  ([T] W4A8 bucket kernels,  */
-/* Int4QuantizedGemmPrecisionTest)                                      */
+/* W4A8: symmetric int8 activations, one scale per (row, group of 32)   */
+/* ([T] W4A8 bucket kernels, Int4QuantizedGemmPrecisionTest)            */
 /* ------------------------------------------------------------------ */
 
-/* Per row m, in IEEE fp32 (round to nearest even):
- *   a = max_k |x[m,k]|,  sx = a / 127,
- *   xq[m,k] = clamp(rint(x[m,k] / sx), -127, 127),  xq = 0 when a == 0.
- * fp32 is the precision of the decision on both sides: x / sx with an
- * fp32 sx can fall within an fp64 rounding of a half-integer. */
+/* Per row m and group g of 32 columns, in IEEE fp32 (round to nearest even):
+ *   a = max_{k in g} |x[m,k]|,  sx[m,g] = a / 127,
+ *   xq[m,k] = clamp(rint(x[m,k] / sx[m,g]), -127, 127),  xq = 0 when a == 0.
+ * One scale per group keeps an outlier channel from flattening the rest of
+ * its row (the precision test's outlier case fails with one scale per row).
+ * fp32 is the precision of the decision on both sides: x / sx with an fp32
+ * sx can fall within an fp64 rounding of a half-integer. */
 void oracle_act_quant(const uint16_t *x, int64_t M, int64_t K, int8_t *xq,
                       float *sx)
 {
-    for (int64_t m = 0; m < M; ++m) {
-        float a = 0.0f;
-        for (int64_t k = 0; k < K; ++k) {
-            float v = fabsf(bf16_to_float(x[m * K + k]));
-            if (v > a)
-                a = v;
-        }
-        volatile float sxm = a / 127.0f;
-        sx[m] = sxm;
-        for (int64_t k = 0; k < K; ++k) {
-            if (a == 0.0f) {
-                xq[m * K + k] = 0;
-                continue;
+    int64_t G = K / GROUP;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t g = 0; g < G; ++g) {
+            float a = 0.0f;
+            for (int64_t i = 0; i < GROUP; ++i) {
+                float v = fabsf(bf16_to_float(x[m * K + g * GROUP + i]));
+                if (v > a)
+                    a = v;
             }
-            volatile float t = bf16_to_float(x[m * K + k]) / sxm;
-            float r = rintf(t);
-            if (r > 127.0f)
-                r = 127.0f;
-            if (r < -127.0f)
-                r = -127.0f;
-            xq[m * K + k] = (int8_t)r;
+            volatile float sxg = a / 127.0f;
+            sx[m * G + g] = sxg;
+            for (int64_t i = 0; i < GROUP; ++i) {
+                int64_t k = g * GROUP + i;
+                if (a == 0.0f) {
+                    xq[m * K + k] = 0;
+                    continue;
+                }
+                volatile float t = bf16_to_float(x[m * K + k]) / sxg;
+                float r = rintf(t);
+                if (r > 127.0f)
+                    r = 127.0f;
+                if (r < -127.0f)
+                    r = -127.0f;
+                xq[m * K + k] = (int8_t)r;
+            }
         }
-    }
 }
 
 /* D[m][n][g] = sum_{k in group g} (q[n,k] - z[n,g]) * xq[m,k], exact int. */
@@ -351,7 +356,7 @@ void oracle_w4a8_group_dots(const int8_t *xq, const uint8_t *q,
             }
 }
 
-/* out[m, n - n0] = sx[m] * sum_g s[n,g] * D[m][n][g] in fp64. */
+/* out[m, n - n0] = sum_g sx[m,g] * s[n,g] * D[m][n][g] in fp64. */
 void oracle_w4a8(const int8_t *xq, const float *sx, const uint8_t *q,
                  const uint16_t *s, const uint8_t *z, int64_t M, int64_t N,
                  int64_t K, int64_t n0, int64_t n1, double *out)
@@ -369,9 +374,9 @@ void oracle_w4a8(const int8_t *xq, const float *sx, const uint8_t *q,
                     d += ((int64_t)q[n * K + k] - (int64_t)z[n * G + g]) *
                          (int64_t)xq[m * K + k];
                 }
-                acc += bf16_to_double(s[n * G + g]) * (double)d;
+                acc += (double)sx[m * G + g] * bf16_to_double(s[n * G + g]) * (double)d;
             }
-            out[m * W + (n - n0)] = (double)sx[m] * acc;
+            out[m * W + (n - n0)] = acc;
         }
 }
 

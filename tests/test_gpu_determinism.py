@@ -18,7 +18,8 @@ def test_graph_replay_matches_eager(cuda, M):
     W8, sc, _ = workloads.w8_inputs(N=N, K=K, M=1, seed=5)
     W8, sc = W8.to(cuda), sc.to(cuda)
     x8 = x[: min(M, 4)].contiguous()
-    eager = (w4q.w4a16_gemm(x, packed, N, K), w4q.w4a8_gemm(x, packed, N, K),
+    xa8 = x[: min(M, 8)].contiguous()          # W4A8 serves up to 8 rows
+    eager = (w4q.w4a16_gemm(x, packed, N, K), w4q.w4a8_gemm(xa8, packed, N, K),
              w4q.w8_gemv(x8, W8, sc))
     ws = torch.empty(max(w4q.workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=cuda)
     outs = (torch.empty_like(eager[0]), torch.empty_like(eager[1]), torch.empty_like(eager[2]))
@@ -32,7 +33,7 @@ def test_graph_replay_matches_eager(cuda, M):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         w4q.w4a16_gemm(x, packed, N, K, out=outs[0], workspace=ws)
-        w4q.w4a8_gemm(x, packed, N, K, out=outs[1], workspace=ws)
+        w4q.w4a8_gemm(xa8, packed, N, K, out=outs[1], workspace=ws)
         w4q.w8_gemv(x8, W8, sc, out=outs[2])
     for o in outs:
         o.zero_()
@@ -51,5 +52,6 @@ def test_repeated_calls_are_bitwise_equal(cuda):
             a = w4q.w4a16_gemm(x, packed, N, K, split_k=split)
             b = w4q.w4a16_gemm(x, packed, N, K, split_k=split)
             assert torch.equal(a, b)
-        assert torch.equal(w4q.w4a8_gemm(x, packed, N, K), w4q.w4a8_gemm(x, packed, N, K))
+        if M <= 8:
+            assert torch.equal(w4q.w4a8_gemm(x, packed, N, K), w4q.w4a8_gemm(x, packed, N, K))
     assert w4q.device_error() == 0
