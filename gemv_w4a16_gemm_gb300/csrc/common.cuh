@@ -103,15 +103,18 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
+#ifndef W4Q_SLEEP_NS
+#define W4Q_SLEEP_NS 20000u
+#endif
 // Wait for the phase of `parity`, the thread sleeping in the instruction
-// (at most 20 us per poll) instead of spinning, so waiting warps leave the
-// issue slots to the others; false after WAIT_LIMIT_NS.
+// (at most W4Q_SLEEP_NS per poll) instead of spinning, so waiting warps
+// leave the issue slots to the others; false after WAIT_LIMIT_NS.
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_timer();
-    while (!mbar_try_wait_sleep(bar, parity, 20000u))
+    while (!mbar_try_wait_sleep(bar, parity, W4Q_SLEEP_NS))
         if (global_timer() - t0 > WAIT_LIMIT_NS)
             return false;
     return true;

@@ -24,9 +24,10 @@
 //   * D (fp32, 128 lanes x NP columns per tile group) accumulates in tensor
 //     memory over the CTA's whole K range and is read once by the epilogue.
 //
-// One CTA per SM, 15 warps: a producer (bulk copies), two MMA issuers (one
-// thread per tile group of the pair; warp 1 also owns the TMEM allocation),
-// four epilogue warps (one per TMEM lane quarter) and eight dequant warps.  A work unit is a pair of tile
+// One CTA per SM, 16 warps: two producers (bulk copies of the codes, and of
+// the activation stages), two MMA issuers (one thread per tile group of the
+// pair; warp 1 also owns the TMEM allocation), four epilogue warps (one per
+// TMEM lane quarter) and eight dequant warps.  A work unit is a pair of tile
 // groups (256 rows) x one 256-K super-block: both groups share one copy of
 // the activation stage.  Units are split into P contiguous ranges (stream-K,
 // or a fixed split of each pair's K); a pair that one CTA covers entirely is
@@ -39,16 +40,17 @@
 // Bounds (derived for every launch the plan can make): packed sources stay
 // below ceil(N/128) * 8 * KB * 2432 bytes (group 2gp + 1 of a pair is
 // copied only when 2gp + 1 < G); activation sources below KB * NP * 512;
-// shared-memory stages inside S * stage bytes of a 1024-aligned base; TMEM
-// columns below 512 (accumulators [0, 256), A slots 256 + 64k + 32g + 8j
-// + 8 <= 512); partial indices below P * 2 * M * 256; outputs only for
+// shared-memory rings inside [SX x (NP x 512)][SW x 38912] of a 1024-aligned base; TMEM
+// columns below 512 (accumulators [0, 256), A slot k sub-block h at
+// 256 + 64 (SPS k + h) + 32g + 8j, + 8 <= 512); partial indices below P * 2 * M * 256; outputs only for
 // n < N and m < M.
 //
 // Pipelines (every wait sleeps in mbarrier.try_wait and gives up after one
 // second of %globaltimer):
-//   producer --full[s]--> dequant + MMA      (packed codes and x of stage s)
-//   dequant  --empty[s]-> producer           (codes read into registers)
-//   MMA      --empty[s]-> producer           (tcgen05.commit: x no longer read)
+//   codes producer --wfull[s]--> dequant     (packed codes of both groups, unit i)
+//   dequant        --wempty[s]-> producer    (codes read into registers)
+//   x producer     --xfull[t]--> MMA         (the activation stage of unit i)
+//   MMA            --xempty[t]-> x producer  (tcgen05.commit: x no longer read)
 //   dequant  --afull[k]-> MMA                (A slot k written to TMEM)
 //   MMA      --aempty[k]-> dequant           (tcgen05.commit: slot k consumed)
 //   MMA      --dfull[d]-> epilogue           (the pair's accumulators final)
@@ -75,7 +77,8 @@ constexpr int UT_GPW = 16 / UT_DQ_WARPS;         // tile groups per dequant warp
 constexpr int UT_FIRST_EPI = 2;
 constexpr int UT_FIRST_DQ = UT_FIRST_EPI + UT_EPI_WARPS;
 constexpr int UT_MMA1 = UT_FIRST_DQ + UT_DQ_WARPS;             // MMA issuer of group 1
-constexpr int UT_THREADS = (UT_MMA1 + 1) * 32;
+constexpr int UT_XPROD = UT_MMA1 + 1;                           // producer of the x ring
+constexpr int UT_THREADS = (UT_XPROD + 1) * 32;
 #ifndef W4Q_UMMA_NDB
 #define W4Q_UMMA_NDB 2
 #endif
@@ -83,7 +86,13 @@ constexpr int UT_NDB = W4Q_UMMA_NDB;  // accumulator buffers (pairs in flight)
 constexpr uint32_t UT_TMEM_COLS = 512;
 constexpr uint32_t UT_DCOL = 128;    // columns per accumulator buffer (2 groups x NP <= 128)
 constexpr uint32_t UT_ACOL = UT_DCOL * UT_NDB;              // first A column
-constexpr int UT_NA = (int)((UT_TMEM_COLS - UT_ACOL) / 64);  // A slots (64-K sub-block, both groups)
+#ifndef W4Q_UMMA_SPS
+#define W4Q_UMMA_SPS 2
+#endif
+// An A slot holds SPS 64-K sub-blocks of both groups: the dequant warps
+// synchronise with the MMA issuers once per slot.
+constexpr int UT_SPS = W4Q_UMMA_SPS;
+constexpr int UT_NA = (int)((UT_TMEM_COLS - UT_ACOL) / (64 * UT_SPS));  // A slots
 constexpr int UT_SMEM_LIMIT = 227 * 1024;
 
 struct UParams {
@@ -96,17 +105,23 @@ struct UParams {
     long long U;
 };
 
+// Two rings: the codes of a unit (both groups, 38912 B) are released as soon
+// as the dequant warps hold them in registers, so that ring can run several
+// units ahead and keep HBM busy; the activation stage (NP x 512 B, from L2)
+// is released by the MMAs' commit.
+constexpr int UT_CODE_BYTES = 2 * UT_GROUP_BYTES;
+
 template <int NP>
-__host__ __device__ constexpr int ut_stage_bytes()
+__host__ __device__ constexpr int ut_xstages()
 {
-    return NP * 512 + 2 * UT_GROUP_BYTES;  // [x: NP x 512][codes of group 0][of group 1]
+    return NP <= 16 ? 3 : 2;
 }
 
 template <int NP>
-__host__ __device__ constexpr int ut_stages()
+__host__ __device__ constexpr int ut_wstages()
 {
-    int s = 4;
-    while (s > 2 && s * ut_stage_bytes<NP>() + 1024 + 512 > UT_SMEM_LIMIT)
+    int s = 6;
+    while (s > 2 && s * UT_CODE_BYTES + ut_xstages<NP>() * NP * 512 + 2048 > UT_SMEM_LIMIT)
         --s;
     return s;
 }
@@ -114,7 +129,8 @@ __host__ __device__ constexpr int ut_stages()
 template <int NP>
 __host__ __device__ constexpr int ut_smem()
 {
-    return ut_stages<NP>() * ut_stage_bytes<NP>() + 1024;  // + alignment slack
+    // [x ring][codes ring] + alignment slack
+    return ut_xstages<NP>() * NP * 512 + ut_wstages<NP>() * UT_CODE_BYTES + 1024;
 }
 
 __host__ __device__ __forceinline__ long long ut_range_begin(const UParams &p, int c)
@@ -151,13 +167,13 @@ __device__ __forceinline__ void ut_dequant_word(uint32_t w, uint32_t zr, uint32_
 template <int NP>
 __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
 {
-    constexpr int S = ut_stages<NP>();
-    constexpr int SB = ut_stage_bytes<NP>();
+    constexpr int SW = ut_wstages<NP>();  // codes ring
+    constexpr int SX = ut_xstages<NP>();  // activation ring
     constexpr uint32_t IDESC = idesc_bf16_f32(128, NP);
     constexpr int XB = NP * 512;  // activation bytes of one stage
 
     extern __shared__ uint8_t ut_dsmem[];
-    __shared__ __align__(8) uint64_t bars[2 * S + 2 * UT_NA + 5];
+    __shared__ __align__(8) uint64_t bars[2 * SW + 2 * SX + 2 * UT_NA + 5];
     __shared__ uint32_t tmem_slot;
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(ut_dsmem) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -169,18 +185,27 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
     const int n_iter = (int)(u1 - u0);
     const int gp_first = (int)(u0 / p.KB), b_first = (int)(u0 % p.KB);
 
-    const uint32_t full0 = smem_addr(&bars[0]);
-    const uint32_t empty0 = smem_addr(&bars[S]);
-    const uint32_t afull0 = smem_addr(&bars[2 * S]);
-    const uint32_t aempty0 = smem_addr(&bars[2 * S + UT_NA]);
-    const uint32_t dfull0 = smem_addr(&bars[2 * S + 2 * UT_NA]);       // [2]
-    const uint32_t dempty0 = smem_addr(&bars[2 * S + 2 * UT_NA + 2]);  // [2]
-    const uint32_t mdone = smem_addr(&bars[2 * S + 2 * UT_NA + 4]);
+    constexpr int B0 = 2 * SW + 2 * SX;
+    const uint32_t wfull0 = smem_addr(&bars[0]);
+    const uint32_t wempty0 = smem_addr(&bars[SW]);
+    const uint32_t xfull0 = smem_addr(&bars[2 * SW]);
+    const uint32_t xempty0 = smem_addr(&bars[2 * SW + SX]);
+    const uint32_t afull0 = smem_addr(&bars[B0]);
+    const uint32_t aempty0 = smem_addr(&bars[B0 + UT_NA]);
+    const uint32_t dfull0 = smem_addr(&bars[B0 + 2 * UT_NA]);       // [2]
+    const uint32_t dempty0 = smem_addr(&bars[B0 + 2 * UT_NA + 2]);  // [2]
+    const uint32_t mdone = smem_addr(&bars[B0 + 2 * UT_NA + 4]);
+    uint8_t *const xring = smem;                // SX x (NP x 512 B), 1024-aligned
+    uint8_t *const wring = smem + SX * XB;      // SW x 38912 B
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, UT_DQ_WARPS + 2);
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(wfull0 + 8 * s, 1);
+            mbar_init(wempty0 + 8 * s, UT_DQ_WARPS);
+        }
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(xfull0 + 8 * s, 1);
+            mbar_init(xempty0 + 8 * s, 2);
         }
         for (int k = 0; k < UT_NA; ++k) {
             mbar_init(afull0 + 8 * k, UT_DQ_WARPS);
@@ -203,53 +228,26 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
+        // ----------------------------------------------- producer of the codes
         if (lane == 0 && n_iter > 0) {
-            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            auto has_g1 = [&](int gp) { return 2 * gp + 1 < p.G; };
-            auto issue_w = [&](int i, int gp, int b) {
-                const int slot = i % S;
-                const uint32_t bar = full0 + 8 * slot;
-                const uint32_t dst = smem_addr(smem + slot * SB + XB);
-                const bool g1 = has_g1(gp);
-                mbar_arrive_expect_tx(bar, (uint32_t)(XB + (g1 ? 2 : 1) * UT_GROUP_BYTES));
+            const uint64_t pol_w = policy_evict_first();
+            int gp = gp_first, b = b_first, issued = 0;
+            for (int i = 0; i < n_iter; ++i) {
+                const int slot = i % SW;
+                if (i >= SW && !mbar_wait_sleep(wempty0 + 8 * slot, (uint32_t)((i / SW) - 1) & 1u)) {
+                    report_error(p.err, ERR_EMPTY_WAIT);
+                    break;
+                }
+                const uint32_t bar = wfull0 + 8 * slot;
+                const uint32_t dst = smem_addr(wring + slot * UT_CODE_BYTES);
+                const bool g1 = 2 * gp + 1 < p.G;
+                mbar_arrive_expect_tx(bar, (uint32_t)((g1 ? 2 : 1) * UT_GROUP_BYTES));
                 bulk_g2s(dst, p.packed + ((size_t)(2 * gp) * p.KB + b) * UT_GROUP_BYTES,
                          UT_GROUP_BYTES, bar, pol_w);
                 if (g1)
                     bulk_g2s(dst + UT_GROUP_BYTES,
                              p.packed + ((size_t)(2 * gp + 1) * p.KB + b) * UT_GROUP_BYTES,
                              UT_GROUP_BYTES, bar, pol_w);
-            };
-            auto issue_x = [&](int i, int b) {
-                const int slot = i % S;
-                bulk_g2s(smem_addr(smem + slot * SB), p.xs + (size_t)b * XB, XB,
-                         full0 + 8 * slot, pol_x);
-            };
-            const int pro = n_iter < S ? n_iter : S;
-            int gp = gp_first, b = b_first;
-            for (int i = 0; i < pro; ++i) {
-                issue_w(i, gp, b);
-                if (++b == p.KB) {
-                    b = 0;
-                    ++gp;
-                }
-            }
-            pdl_wait();  // x comes from act_prep, launched just before
-            int xb = b_first;
-            for (int i = 0; i < pro; ++i) {
-                issue_x(i, xb);
-                if (++xb == p.KB)
-                    xb = 0;
-            }
-            int issued = pro;
-            for (int i = pro; i < n_iter; ++i) {
-                const int slot = i % S;
-                if (!mbar_wait_sleep(empty0 + 8 * slot, (uint32_t)((i / S) - 1) & 1u)) {
-                    report_error(p.err, ERR_EMPTY_WAIT);
-                    break;
-                }
-                issue_w(i, gp, b);
-                issue_x(i, b);
                 issued = i + 1;
                 if (++b == p.KB) {
                     b = 0;
@@ -257,8 +255,33 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                 }
             }
             // drain: every issued copy has landed before the CTA exits
-            for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-                if (!mbar_wait_sleep(full0 + 8 * (i % S), (uint32_t)(i / S) & 1u)) {
+            for (int i = (issued > SW ? issued - SW : 0); i < issued; ++i)
+                if (!mbar_wait_sleep(wfull0 + 8 * (i % SW), (uint32_t)(i / SW) & 1u)) {
+                    report_error(p.err, ERR_DRAIN_WAIT);
+                    break;
+                }
+        }
+    } else if (warp == UT_XPROD) {
+        // ------------------------------------------- producer of the x stages
+        if (lane == 0 && n_iter > 0) {
+            const uint64_t pol_x = policy_evict_last();
+            pdl_wait();  // x comes from act_prep, launched just before
+            int b = b_first, issued = 0;
+            for (int i = 0; i < n_iter; ++i) {
+                const int slot = i % SX;
+                if (i >= SX && !mbar_wait_sleep(xempty0 + 8 * slot, (uint32_t)((i / SX) - 1) & 1u)) {
+                    report_error(p.err, ERR_EMPTY_WAIT);
+                    break;
+                }
+                const uint32_t bar = xfull0 + 8 * slot;
+                mbar_arrive_expect_tx(bar, (uint32_t)XB);
+                bulk_g2s(smem_addr(xring + slot * XB), p.xs + (size_t)b * XB, XB, bar, pol_x);
+                issued = i + 1;
+                if (++b == p.KB)
+                    b = 0;
+            }
+            for (int i = (issued > SX ? issued - SX : 0); i < issued; ++i)
+                if (!mbar_wait_sleep(xfull0 + 8 * (i % SX), (uint32_t)(i / SX) & 1u)) {
                     report_error(p.err, ERR_DRAIN_WAIT);
                     break;
                 }
@@ -275,8 +298,8 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             int a_it = 0, d_it = 0, gp = gp_first, b = b_first;
             bool first = true, ok = true;
             for (int i = 0; i < n_iter && ok; ++i) {
-                const int slot = i % S;
-                if (!mbar_wait_sleep(full0 + 8 * slot, (uint32_t)(i / S) & 1u) ||
+                const int slot = i % SX;
+                if (!mbar_wait_sleep(xfull0 + 8 * slot, (uint32_t)(i / SX) & 1u) ||
                     (first && !mbar_wait_sleep(dempty0 + 8 * (d_it % UT_NDB),
                                                  (uint32_t)((d_it / UT_NDB) & 1) ^ 1u))) {
                     report_error(p.err, ERR_FULL_WAIT);
@@ -286,8 +309,8 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                 tc_fence_after_sync();
                 const bool live = gi == 0 || 2 * gp + 1 < p.G;
                 const uint32_t d_tmem = tmem + UT_DCOL * (uint32_t)(d_it % UT_NDB) + (uint32_t)(gi * NP);
-                const uint64_t bdesc = sdesc_sw128_kmajor(smem_addr(smem + slot * SB));
-                for (int sbk = 0; sbk < 4; ++sbk) {
+                const uint64_t bdesc = sdesc_sw128_kmajor(smem_addr(xring + slot * XB));
+                for (int s0 = 0; s0 < 4; s0 += UT_SPS) {  // one A slot: UT_SPS sub-blocks
                     const int k = a_it % UT_NA;
                     if (!mbar_wait_sleep(afull0 + 8 * k, (uint32_t)(a_it / UT_NA) & 1u)) {
                         report_error(p.err, ERR_FULL_WAIT);
@@ -296,21 +319,26 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                     }
                     tc_fence_after_sync();
                     if (live) {
-                        const uint32_t a_tmem = tmem + UT_ACOL + (uint32_t)(64 * k + 32 * gi);
-                        // the start-address field (bits 0..13, bytes / 16) advances
-                        // by one sub-block of rows, then by 32 bytes per K step
-                        const uint64_t bd = bdesc + (uint64_t)((sbk * NP * 128) >> 4);
-                        umma_ts(d_tmem, a_tmem, bd, IDESC, (first && sbk == 0) ? 0u : 1u);
-                        umma_ts(d_tmem, a_tmem + 8, bd + 2, IDESC, 1u);
-                        umma_ts(d_tmem, a_tmem + 16, bd + 4, IDESC, 1u);
-                        umma_ts(d_tmem, a_tmem + 24, bd + 6, IDESC, 1u);
+#pragma unroll
+                        for (int h = 0; h < UT_SPS; ++h) {
+                            const int sbk = s0 + h;
+                            const uint32_t a_tmem =
+                                tmem + UT_ACOL + (uint32_t)(64 * (UT_SPS * k + h) + 32 * gi);
+                            // the start-address field (bits 0..13, bytes / 16) advances
+                            // by one sub-block of rows, then by 32 bytes per K step
+                            const uint64_t bd = bdesc + (uint64_t)((sbk * NP * 128) >> 4);
+                            umma_ts(d_tmem, a_tmem, bd, IDESC, (first && sbk == 0) ? 0u : 1u);
+                            umma_ts(d_tmem, a_tmem + 8, bd + 2, IDESC, 1u);
+                            umma_ts(d_tmem, a_tmem + 16, bd + 4, IDESC, 1u);
+                            umma_ts(d_tmem, a_tmem + 24, bd + 6, IDESC, 1u);
+                        }
                     }
                     umma_commit(aempty0 + 8 * k);
                     ++a_it;
                 }
                 if (!ok)
                     break;
-                umma_commit(empty0 + 8 * slot);
+                umma_commit(xempty0 + 8 * slot);  // the x stage is no longer read
                 first = false;
                 if (++b == p.KB || i == n_iter - 1) {  // the pair's last unit in this range
                     umma_commit(dfull0 + 8 * (d_it % UT_NDB));
@@ -392,13 +420,13 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
         int a_it = 0, gp = gp_first, b = b_first, pend = -1;
         bool ok = true;
         for (int i = 0; i < n_iter && ok; ++i) {
-            const int slot = i % S;
-            if (!mbar_wait_sleep(full0 + 8 * slot, (uint32_t)(i / S) & 1u)) {
+            const int slot = i % SW;
+            if (!mbar_wait_sleep(wfull0 + 8 * slot, (uint32_t)(i / SW) & 1u)) {
                 report_error(p.err, ERR_FULL_WAIT);
                 break;
             }
             const int ng = (2 * gp + 1 < p.G) ? 2 : 1;
-            const uint32_t tbase = smem_addr(smem + slot * SB + XB + tl * UT_TILE_BYTES);
+            const uint32_t tbase = smem_addr(wring + slot * UT_CODE_BYTES + tl * UT_TILE_BYTES);
             uint4 wq[UT_GPW][4], sc0[UT_GPW], sc1[UT_GPW], zz[UT_GPW];
 #pragma unroll
             for (int gg = 0; gg < UT_GPW; ++gg)
@@ -413,7 +441,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                 }
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(empty0 + 8 * slot);  // the stage's codes are in registers
+                mbar_arrive(wempty0 + 8 * slot);  // the unit's codes are in registers
 #pragma unroll
             for (int sbk = 0; sbk < 4; ++sbk) {
                 uint32_t v[UT_GPW][16];
@@ -438,28 +466,34 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
                             ut_dequant_word(wv[j], zr, zr8, s2r, s2r8, &v[gg][4 * j]);
                         }
                     }
-                if (pend >= 0) {
-                    tmem_wait_st();
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(afull0 + 8 * pend);
-                    pend = -1;
-                }
                 const int k = a_it % UT_NA;
-                if (!mbar_wait_sleep(aempty0 + 8 * k, ((uint32_t)(a_it / UT_NA) & 1u) ^ 1u)) {
-                    report_error(p.err, ERR_EMPTY_WAIT);
-                    ok = false;
-                    break;
+                if (sbk % UT_SPS == 0) {  // the first sub-block of a slot
+                    if (pend >= 0) {      // the previous slot's stores: complete, then publish
+                        tmem_wait_st();
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(afull0 + 8 * pend);
+                        pend = -1;
+                    }
+                    if (!mbar_wait_sleep(aempty0 + 8 * k, ((uint32_t)(a_it / UT_NA) & 1u) ^ 1u)) {
+                        report_error(p.err, ERR_EMPTY_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
                 }
-                tc_fence_after_sync();
 #pragma unroll
                 for (int gg = 0; gg < UT_GPW; ++gg)
                     if (g0 + gg < ng)
-                        tmem_st_16x256b_x4(
-                            tmem + tlane + UT_ACOL + (uint32_t)(64 * k + 32 * (g0 + gg)), v[gg]);
-                pend = k;
-                ++a_it;
+                        tmem_st_16x256b_x4(tmem + tlane + UT_ACOL +
+                                               (uint32_t)(64 * (UT_SPS * k + sbk % UT_SPS) +
+                                                          32 * (g0 + gg)),
+                                           v[gg]);
+                if (sbk % UT_SPS == UT_SPS - 1) {
+                    pend = k;
+                    ++a_it;
+                }
             }
             if (++b == p.KB) {
                 b = 0;
