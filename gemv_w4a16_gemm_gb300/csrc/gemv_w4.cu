@@ -57,6 +57,14 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// Ring waits of this file: sleeping in mbarrier.try_wait (the default) or
+// spinning on it.
+#ifdef W4Q_SPIN_WAITS
+#define W4Q_RING_WAIT mbar_wait_bounded
+#else
+#define W4Q_RING_WAIT mbar_wait_sleep
+#endif
+
 namespace w4q {
 
 namespace {
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                     xb = 0;
             }
             issued = first;
-            if (pro > first && !mbar_wait_bounded(full0, 0u))
+            if (pro > first && !W4Q_RING_WAIT(full0, 0u))
                 report_error(p.err, ERR_FULL_WAIT);
             for (int i = first; i < pro; ++i) {
                 issue_w(i, g, b);
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             for (int i = pro; i < n_iter; ++i) {
                 const int slot = i % STAGES;
                 const uint32_t use = (uint32_t)(i / STAGES);
-                if (!mbar_wait_bounded(empty0 + 8 * slot, (use - 1) & 1)) {
+                if (!W4Q_RING_WAIT(empty0 + 8 * slot, (use - 1) & 1)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
                 }
@@ -568,7 +576,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 cur_g = g;
             }
             const int slot = i % STAGES;
-            if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / STAGES) & 1)) {
+            if (!W4Q_RING_WAIT(full0 + 8 * slot, (uint32_t)(i / STAGES) & 1)) {
                 report_error(p.err, ERR_FULL_WAIT);
                 ok = false;
                 break;
@@ -605,7 +613,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     if (warp == WARPS && lane == 0) {
         for (int s = 0; s < STAGES && s < issued; ++s) {
             const int last_use = (issued - 1 - s) / STAGES;
-            if (!mbar_wait_bounded(full0 + 8 * s, (uint32_t)last_use & 1)) {
+            if (!W4Q_RING_WAIT(full0 + 8 * s, (uint32_t)last_use & 1)) {
                 report_error(p.err, ERR_DRAIN_WAIT);
                 break;
             }

@@ -24,6 +24,14 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// Ring waits of this file: sleeping in mbarrier.try_wait (the default) or
+// spinning on it.
+#ifdef W4Q_SPIN_WAITS
+#define W4Q_RING_WAIT mbar_wait_bounded
+#else
+#define W4Q_RING_WAIT mbar_wait_sleep
+#endif
+
 namespace w4q {
 
 namespace {
@@ -76,7 +84,7 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
             for (int i = 0; i < n_iter; ++i) {
                 const int slot = i % STAGES;
                 if (i >= STAGES &&
-                    !mbar_wait_bounded(empty0 + 8 * slot, (uint32_t)(i / STAGES - 1) & 1)) {
+                    !W4Q_RING_WAIT(empty0 + 8 * slot, (uint32_t)(i / STAGES - 1) & 1)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
                 }
@@ -116,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
         }
         for (int i = 0; i < n_iter; ++i) {
             const int slot = i % STAGES;
-            if (!mbar_wait_bounded(full0 + 8 * slot, (uint32_t)(i / STAGES) & 1)) {
+            if (!W4Q_RING_WAIT(full0 + 8 * slot, (uint32_t)(i / STAGES) & 1)) {
                 report_error(p.err, ERR_FULL_WAIT);
                 break;
             }
@@ -184,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
     if (warp == CWARPS && lane == 0) {
         for (int s = 0; s < STAGES && s < issued; ++s) {
             const int last_use = (issued - 1 - s) / STAGES;
-            if (!mbar_wait_bounded(full0 + 8 * s, (uint32_t)last_use & 1)) {
+            if (!W4Q_RING_WAIT(full0 + 8 * s, (uint32_t)last_use & 1)) {
                 report_error(p.err, ERR_DRAIN_WAIT);
                 break;
             }
