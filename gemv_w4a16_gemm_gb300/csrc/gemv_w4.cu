@@ -8,31 +8,42 @@
 // bucket kernels and the W4A16 tile kernels; this is a new design for GB300,
 // not their code.)
 //
-// Two launches per call, both with programmatic dependent launch: act_prep
-// starts while the previous kernel on the stream finishes (it waits for it in
-// griddepcontrol.wait before reading x), and the main kernel starts
-// streaming weights while act_prep runs.
-//  1. act_prep (a few CTAs per activation row) prepares the activation operand
-//     in the workspace, super-block-major ([K/256][M][256 + 8 pad] bf16 and
-//     [K/256][M][8] fp32, so one bulk copy moves a stage's rows), and zeroes
-//     the split-K counters:
-//       W4A16:  x' = x * 2^sigma, with an extra 2^-4 on the upper eight
-//               columns of every 16-column step (sigma from max|x|, so x'
-//               stays finite); X'[g] = 2^(sigma-133) * sum_{k in g} x_k;
-//               out scale 2^(133 - sigma).
-//       W4A8:   sx = fp32(max|x| / 127), xq = clamp(rint(fp32(x / sx))),
-//               x' = xq * 2^121 (2^117 on upper halves), X'[g] =
-//               2^-12 * sum xq (exact), out scale sx * 2^12.
-//  2. w4_kernel (launched with programmatic dependent launch, so it starts
-//     streaming weights while act_prep runs): one CTA = 8 consumer warps +
-//     1 producer warp.
+// Two launches per call, both with programmatic dependent launch: each
+// starts while the kernel before it on the stream finishes and waits for it
+// in griddepcontrol.wait before it reads anything that kernel wrote.
+//  1. A prologue that zeroes the split-K counters.  Except for W4A16 at
+//     M <= 2 (see below), it (act_prep, a few CTAs per activation row) also
+//     prepares the activation operand in the workspace, super-block-major
+//     ([K/256][M][256 + 8 pad] bf16 and [K/256][M][8] fp32, so one bulk copy
+//     moves a stage's rows):
+//       W4A16:  per row and 256-column super-block, x' = x * 2^sigma (the
+//               W4A16 rule below), X', and the row factor c;
+//       W4A8:   sx = fp32(max|x| / 127) per (row, group of 32),
+//               xq = clamp(rint(fp32(x / sx))), x' = xq * 2^121 (2^117 on
+//               upper halves), X'[g] = 2^-12 * sum xq (exact), group scale
+//               sx * 2^12.
+//  2. w4_kernel (it starts streaming weights while the prologue runs): one
+//     CTA = 8 consumer warps + 1 producer warp.
 //       * The weight is read once: each stage is one 19456-byte bulk copy
 //         (TMA engine) of the 8 packed tiles (16 rows x 256 K: codes,
 //         scales, zeros) of a 128-row group, plus one copy each of the
-//         matching x' rows and X' slice, into a multi-stage shared-memory
-//         ring guarded by mbarriers (three copies per stage: the TMA issue
-//         rate, about one copy per 70 SM cycles, is a real limit).
-//         Weights carry an L2 evict-first hint, activations evict-last.
+//         matching prepared activation rows, into a multi-stage
+//         shared-memory ring guarded by mbarriers (the TMA issue rate, about
+//         one copy per 70 SM cycles, is a real limit).  Weights carry an L2
+//         evict-first hint, activations evict-last.
+//       * W4A16 activation rule: per row m and 256-column super-block b,
+//         sigma from max |x| over the super-block (so x' stays finite),
+//         x' = x * 2^sigma exactly, with an extra 2^-4 on the upper eight
+//         columns of every 16-column step, X'[g] = 2^(sigma-133) *
+//         sum_{k in g} x_k, and c = 2^(133 - sigma), the factor that takes
+//         the super-block's sums back to output units (applied once per
+//         stage).  At M <= 2 the producer warp prepares each stage this way
+//         itself, from x as given (L2-resident, read with plain loads), one
+//         stage behind its weight copies: that keeps two global round trips
+//         and a kernel boundary off the critical path of the call.  At
+//         M >= 3 the preparation would cost the producer warp's scheduler
+//         more than the consumers sharing it can give, so the prologue does
+//         it.
 //       * Consumer warp w owns row tile w of the CTA's 128-row tile group.
 //         A lane's 16 bytes of a sub-block hold its A fragments of four
 //         m16n8k16 MMAs; masking a word with 0x000F000F / 0x00F000F0 turns
@@ -78,14 +89,14 @@ constexpr int SROW = 32;                   // one activation row's 8 group sums 
 
 struct Params {
     const uint8_t *packed;
-    const __nv_bfloat16 *x;  // bf16 [K/256][M][264]: x' (prepared)
-    const float *xsum;       // fp32 [K/256][M][8]: X'
-    const float *gscale;     // fp32 [K/256][M][8]: W4A8 activation scale x 2^12 per group
-    const float *oscale;     // fp32 [M]: output scale per row
+    const __nv_bfloat16 *x;  // W4A8: bf16 [K/256][M][264]: x' (prepared)
+    const float *xsum;       // W4A8: fp32 [K/256][M][8]: X'
+    const float *gscale;     // W4A8: fp32 [K/256][M][8]: activation scale x 2^12 per group
+    const __nv_bfloat16 *xin;  // W4A16: bf16 [M][K], the activations as given
     __nv_bfloat16 *out;      // bf16 [M][N]
     int32_t *dots;           // group-dot export: int32 [M][N][K/32]
     float *partial;          // fp32 [P][2][M][GROUP_ROWS]
-    unsigned *counters;      // [G][WARPS] arrivals per row tile (zeroed by act_prep)
+    unsigned *counters;      // [G][WARPS] arrivals per row tile (zeroed by the prologue)
     unsigned *err;
     int M, N, K, KB, T, G, P, split;
     long long U;
@@ -108,11 +119,22 @@ __device__ __forceinline__ int range_owner(const Params &p, long long u)
     return g * p.split + (int)(((long long)(b + 1) * p.split - 1) / p.KB);
 }
 
+// W4A16 prepares its activation operand inside the main kernel up to this
+// many rows per accumulator slot (MP), in the prologue above.
+#ifndef W4Q_INPREP_MAX_MP
+#define W4Q_INPREP_MAX_MP 2
+#endif
+__host__ __device__ constexpr bool in_kernel_prep(W4Mode mode, int mp)
+{
+    return mode == W4Mode::A16 && mp <= W4Q_INPREP_MAX_MP;
+}
+
 template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int stage_bytes()
 {
-    // codes, x' rows, X' rows, and for W4A8 the per-group activation scales
-    return WARPS * TILE_BYTES + NB * 8 * XROW + NB * 8 * SROW * (MODE == W4Mode::A8 ? 2 : 1);
+    // codes, x' rows, X' rows, and per row the W4A8 group scales (W4A16: the
+    // stage's row factor c in the row's first word)
+    return WARPS * TILE_BYTES + NB * 8 * XROW + NB * 8 * SROW * 2;
 }
 
 template <int NB, W4Mode MODE>
@@ -127,8 +149,9 @@ __host__ __device__ constexpr int stages_for()
 template <int NB, W4Mode MODE>
 __host__ __device__ constexpr int smem_for()
 {
-    // + barriers + a 16-byte zero row (the B rows of the column-packed stage that are zero)
-    return stages_for<NB, MODE>() * stage_bytes<NB, MODE>() + 2 * stages_for<NB, MODE>() * 8 + 16;
+    // + barriers (full, empty) + a 16-byte zero row (the B rows of the
+    // column-packed stage that are zero)
+    return stages_for<NB, MODE>() * stage_bytes<NB, MODE>() + (2 * stages_for<NB, MODE>() * 8 + 15) / 16 * 16 + 16;
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr)
@@ -140,8 +163,9 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 
 // One stage: this warp's 16 x 256 tile, 4 sub-blocks of 64 K (two groups
 // each), 4 k16 steps per sub-block.  xbase: the stage's activation rows;
-// sbase: the stage's group sums.
-template <int NB, bool DOTS, bool GS>
+// sbase: the stage's group sums; gbase: per row, the W4A8 group scales (GS)
+// or the stage's row factor c (SC: the stage's sum is scaled once by c).
+template <int NB, bool DOTS, bool GS, bool SC>
 __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, uint32_t sbase,
                                               uint32_t gbase, int lane, float (&acc)[NB][4],
                                               const Params &p, int tile, int b)
@@ -155,6 +179,11 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
     // ldmatrix.x4 row addresses: matrix lane>>3 = (step +lane>>4, k half (lane>>3)&1)
     const uint32_t xlane = xbase + (lane & 7) * XROW + 32 * (lane >> 4) + 16 * ((lane >> 3) & 1);
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float sacc[NB][4];  // SC: this stage's sums, before the row factors
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+        sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
+    float (&tgt)[NB][4] = SC ? sacc : acc;
 
     // group sums X' of this lane's two output columns, per n8 block
     float xs[NB][2][8];
@@ -234,13 +263,24 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
                         // W4A8: times the activation scale of (column, group)
                         const float g0 = GS ? __uint_as_float(lds32(gbase + (nb * 8 + c2) * SROW + 4 * g)) : 1.f;
                         const float g1 = GS ? __uint_as_float(lds32(gbase + (nb * 8 + c2 + 1) * SROW + 4 * g)) : 1.f;
-                        acc[nb][0] = fmaf(GS ? sr * g0 : sr, fmaf(nzr, xs[nb][0][g], d[nb][0]), acc[nb][0]);
-                        acc[nb][1] = fmaf(GS ? sr * g1 : sr, fmaf(nzr, xs[nb][1][g], d[nb][1]), acc[nb][1]);
-                        acc[nb][2] = fmaf(GS ? sr8 * g0 : sr8, fmaf(nzr8, xs[nb][0][g], d[nb][2]), acc[nb][2]);
-                        acc[nb][3] = fmaf(GS ? sr8 * g1 : sr8, fmaf(nzr8, xs[nb][1][g], d[nb][3]), acc[nb][3]);
+                        tgt[nb][0] = fmaf(GS ? sr * g0 : sr, fmaf(nzr, xs[nb][0][g], d[nb][0]), tgt[nb][0]);
+                        tgt[nb][1] = fmaf(GS ? sr * g1 : sr, fmaf(nzr, xs[nb][1][g], d[nb][1]), tgt[nb][1]);
+                        tgt[nb][2] = fmaf(GS ? sr8 * g0 : sr8, fmaf(nzr8, xs[nb][0][g], d[nb][2]), tgt[nb][2]);
+                        tgt[nb][3] = fmaf(GS ? sr8 * g1 : sr8, fmaf(nzr8, xs[nb][1][g], d[nb][3]), tgt[nb][3]);
                     }
                 }
             }
+        }
+    }
+    if (SC) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const float ca = __uint_as_float(lds32(gbase + (nb * 8 + c2) * SROW));
+            const float cb = __uint_as_float(lds32(gbase + (nb * 8 + c2 + 1) * SROW));
+            acc[nb][0] = fmaf(ca, sacc[nb][0], acc[nb][0]);
+            acc[nb][1] = fmaf(cb, sacc[nb][1], acc[nb][1]);
+            acc[nb][2] = fmaf(ca, sacc[nb][2], acc[nb][2]);
+            acc[nb][3] = fmaf(cb, sacc[nb][3], acc[nb][3]);
         }
     }
 }
@@ -254,8 +294,9 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
 // at the x' row of their column.  One accumulator thus sums the dots of
 // 8 / MP groups side by side, and the fp32 scale / zero update runs once per
 // 8 / MP groups instead of once per group.  The lanes of one accumulator row
-// hold different slots of the same outputs; the flush adds them.
-template <int MP, bool DOTS, bool GS>
+// hold different slots of the same outputs; the flush adds them.  GS, SC: as
+// for compute_stage.
+template <int MP, bool DOTS, bool GS, bool SC>
 __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xbase,
                                                      uint32_t sbase, uint32_t gbase, uint32_t zaddr,
                                                      int lane, float (&acc)[1][4], const Params &p,
@@ -268,6 +309,8 @@ __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xb
     const uint32_t brow = xbase + (bn % MP) * XROW + 32 * (q >> 1) + 16 * (q & 1);
     const int s0 = c2 / MP, s1 = (c2 + 1) / MP, m0 = c2 % MP, m1 = (c2 + 1) % MP;
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};  // SC: this stage's sums, before the row factors
+    float (&tgt)[1][4] = SC ? sacc : acc;
     uint32_t wv[16];  // word of step st: codes of rows r, r + 8 (step = 2 * group + half)
 #pragma unroll
     for (int sbk = 0; sbk < 4; ++sbk) {
@@ -338,12 +381,121 @@ __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xb
             // W4A8: times the activation scale of (row of x, group)
             const float ga = GS ? __uint_as_float(lds32(gbase + m0 * SROW + 4 * g0)) : 1.f;
             const float gb = GS ? __uint_as_float(lds32(gbase + m1 * SROW + 4 * g1)) : 1.f;
-            acc[0][0] = fmaf(bf16lo_to_f32(sp0) * ga, fmaf(nz0, xs0, d[0]), acc[0][0]);
-            acc[0][1] = fmaf(bf16lo_to_f32(sp1) * gb, fmaf(nz1, xs1, d[1]), acc[0][1]);
-            acc[0][2] = fmaf(bf16hi_to_f32(sp0) * ga, fmaf(nz08, xs0, d[2]), acc[0][2]);
-            acc[0][3] = fmaf(bf16hi_to_f32(sp1) * gb, fmaf(nz18, xs1, d[3]), acc[0][3]);
+            tgt[0][0] = fmaf(bf16lo_to_f32(sp0) * ga, fmaf(nz0, xs0, d[0]), tgt[0][0]);
+            tgt[0][1] = fmaf(bf16lo_to_f32(sp1) * gb, fmaf(nz1, xs1, d[1]), tgt[0][1]);
+            tgt[0][2] = fmaf(bf16hi_to_f32(sp0) * ga, fmaf(nz08, xs0, d[2]), tgt[0][2]);
+            tgt[0][3] = fmaf(bf16hi_to_f32(sp1) * gb, fmaf(nz18, xs1, d[3]), tgt[0][3]);
         }
     }
+    if (SC) {
+        const float ca = __uint_as_float(lds32(gbase + m0 * SROW));
+        const float cb = __uint_as_float(lds32(gbase + m1 * SROW));
+        acc[0][0] = fmaf(ca, sacc[0][0], acc[0][0]);
+        acc[0][1] = fmaf(cb, sacc[0][1], acc[0][1]);
+        acc[0][2] = fmaf(ca, sacc[0][2], acc[0][2]);
+        acc[0][3] = fmaf(cb, sacc[0][3], acc[0][3]);
+    }
+}
+
+// W4A16: one stage's activation operand, prepared by the producer warp from
+// super-block b of x (rows m < M, 256 columns; lane l holds columns
+// 8l .. 8l + 7, so an odd lane holds the upper half of a 16-column step).
+// Per row: sigma from max |x| over the super-block, x' = x * 2^sigma (upper
+// halves 2^(sigma - 4)) as bf16, X'[g] = 2^(sigma - 133) * sum_{k in g} x_k,
+// c = 2^(133 - sigma).  sigma keeps |x'| < 2^128, so every power-of-two
+// product below is exact and x' is x scaled without rounding.
+template <int MP>
+__device__ __forceinline__ void load_stage_a16(const __nv_bfloat16 *__restrict__ x, int M, int K,
+                                               int b, int lane, uint4 (&raw)[MP])
+{
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+        raw[m] = m < M ? __ldcg(reinterpret_cast<const uint4 *>(x + (size_t)m * K +
+                                                               (size_t)b * 256) + lane)
+                       : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The MP rows are processed together (rows m >= M hold zeros and are not
+// stored), so that their reduction chains overlap.
+template <int MP>
+__device__ __forceinline__ void prep_stage_a16(const uint4 (&raw)[MP], int M, int lane,
+                                               uint8_t *xdst, uint8_t *sdst, uint8_t *cdst)
+{
+    constexpr int NW = (MP + 1) / 2;
+    // max |x| per row: magnitudes of bf16 numbers order as their bit
+    // patterns; two rows per word (16-bit lanes) for the warp reduction
+    uint32_t mx[NW];
+#pragma unroll
+    for (int j = 0; j < NW; ++j)
+        mx[j] = 0u;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+        const uint32_t h = __vmaxu2(__vmaxu2(raw[m].x & 0x7FFF7FFFu, raw[m].y & 0x7FFF7FFFu),
+                                    __vmaxu2(raw[m].z & 0x7FFF7FFFu, raw[m].w & 0x7FFF7FFFu));
+        mx[m / 2] |= max(h & 0xFFFFu, h >> 16) << (16 * (m & 1));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < NW; ++j)
+            mx[j] = __vmaxu2(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], o));
+    float part[MP];
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+        const uint32_t a = (mx[m / 2] >> (16 * (m & 1))) & 0xFFFFu;
+        // e with max |x| < 2^e (e = 0 for an all-zero row), from the bf16 bits:
+        // a normal number with biased exponent E is below 2^(E - 126); a
+        // subnormal q * 2^-133 with q < 2^nb is below 2^(nb - 133)
+        const int e = a >= 0x80u ? (int)(a >> 7) - 126 : (a != 0u ? (32 - __clz((int)a)) - 133 : 0);
+        const int sigma = min(max(128 - e, 6), 259);
+        const int sh = (lane & 1) ? sigma - 4 : sigma;
+        const uint32_t w[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = bf16lo_to_f32(w[j]);
+            v[2 * j + 1] = bf16hi_to_f32(w[j]);
+        }
+        part[m] = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+        // 2^sh in factors of at most 2^127 (sh <= 259)
+        const float f1 = __uint_as_float((uint32_t)(min(sh, 127) + 127) << 23);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] *= f1;
+        if (sigma > 127) {  // the same for the whole warp
+            const int a2 = min(max(sh - 127, 0), 127);
+            const float f2 = __uint_as_float((uint32_t)(a2 + 127) << 23);
+            const float f3 = __uint_as_float((uint32_t)(max(sh - 254, 0) + 127) << 23);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = v[j] * f2 * f3;
+        }
+        uint32_t ow[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);  // .x low
+            ow[j] = *reinterpret_cast<const uint32_t *>(&h2);
+        }
+        if (m < M) {
+            *reinterpret_cast<uint4 *>(xdst + m * XROW + 16 * lane) =
+                make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            if (lane == 0)
+                *reinterpret_cast<float *>(cdst + m * SROW) =
+                    __uint_as_float((uint32_t)(260 - sigma) << 23);
+        }
+        // 2^(sigma - 133) = 2^(sigma - 132) * 2^-1, both normal for sigma in [6, 259]
+        part[m] *= __uint_as_float((uint32_t)(sigma - 5) << 23);
+    }
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+        part[m] += __shfl_xor_sync(0xffffffffu, part[m], 1);
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+        part[m] += __shfl_xor_sync(0xffffffffu, part[m], 2);
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+        if (m < M && (lane & 3) == 0)
+            *reinterpret_cast<float *>(sdst + m * SROW + 4 * (lane >> 2)) = part[m] * 0.5f;
 }
 
 template <int NB, W4Mode MODE, int MP>
@@ -354,30 +506,38 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     constexpr int SB = stage_bytes<NB, MODE>();
     constexpr int XOFF = WARPS * TILE_BYTES;     // activation rows within a stage
     constexpr int SOFF = XOFF + NB * 8 * XROW;   // group sums within a stage
-    constexpr int GOFF = SOFF + NB * 8 * SROW;   // W4A8 group scales within a stage
+    constexpr int GOFF = SOFF + NB * 8 * SROW;   // group scales / row factors within a stage
+    constexpr bool A16 = MODE == W4Mode::A16;
+    constexpr bool INPREP = in_kernel_prep(MODE, MP);  // x' prepared by the producer warp
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * SB);
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + STAGES);
-    const uint32_t zrow = smem_addr(bars + 2 * STAGES);  // 16 zero bytes
+    constexpr int ZOFF = (2 * STAGES * 8 + 15) / 16 * 16;
+    const uint32_t zrow = smem_addr(smem + STAGES * SB + ZOFF);  // 16 zero bytes
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Hardware warp 0 is the producer (role index WARPS): the schedulers favour
+    // low warp ids, and the W4A16 producer's preparation must not wait behind
+    // eight ready consumer warps.  Hardware warps 1 .. 8 are consumers 0 .. 7.
+    const int hw_warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = hw_warp == 0 ? WARPS : hw_warp - 1;
     const int c = blockIdx.x;
     const long long u0 = range_begin(p, c), u1 = range_begin(p, c + 1);
     const int n_iter = (int)(u1 - u0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            // W4A16: the weight copy's arrival + the producer warp's (x' written)
+            mbar_init(full0 + 8 * s, INPREP ? 2 : 1);
             mbar_init(empty0 + 8 * s, WARPS);
         }
-        *reinterpret_cast<uint4 *>(bars + 2 * STAGES) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(smem + STAGES * SB + ZOFF) = make_uint4(0u, 0u, 0u, 0u);
         fence_barrier_init();
     }
     {   // activation rows m >= M of every stage stay zero (never copied into)
         const int pad_rows = NB * 8 - p.M;
         const int xper = pad_rows * (XROW / 16);
-        const int sper = pad_rows * (SROW / 16) * (MODE == W4Mode::A8 ? 2 : 1);
+        const int sper = pad_rows * (SROW / 16) * 2;
         for (int i = threadIdx.x; i < STAGES * (xper + sper); i += THREADS) {
             const int s = i / (xper + sper), rem = i % (xper + sper);
             uint8_t *dst = rem < xper
@@ -398,11 +558,93 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     const int g_first = (int)(u0 / p.KB), b_first = (int)(u0 % p.KB);
     int issued = 0;
     if (warp == WARPS) {
-        // ------------------------------------------------------- producer
-        if (lane == 0) {
+        if constexpr (INPREP) {
+            // ------------------------------------- producer, W4A16 (whole warp)
+            // Lane 0 issues the weight copies; the warp prepares x' one stage
+            // behind them, from x loaded PD stages ahead of its preparation
+            // (so the load latency stays hidden when the preparation is the
+            // longer path).  Before waiting for slot i the warp has prepared
+            // every stage up to i - 1, so the consumers can always free it.
+            constexpr int PD = MP <= 4 ? 2 : 1;
+            const uint64_t pol_w = policy_evict_first();
+            int g = g_first, b = b_first;   // unit of the next weight copy
+            int tdone = 0;                  // stages prepared
+            int nload = 0, lb = b_first;    // stages loaded; super-block of the next
+            uint4 raw[PD][MP];              // x of stages tdone .. tdone + PD - 1
+            auto issue_w = [&](int i) {
+                if (lane == 0) {
+                    const int slot = i % STAGES;
+                    const uint32_t bar = full0 + 8 * slot;
+                    mbar_arrive_expect_tx(bar, (uint32_t)(WARPS * TILE_BYTES));
+                    bulk_g2s(smem_addr(smem + slot * SB),
+                             p.packed + ((size_t)g * p.KB + b) * (WARPS * TILE_BYTES),
+                             WARPS * TILE_BYTES, bar, pol_w);
+                }
+                if (++b == p.KB) {
+                    b = 0;
+                    ++g;
+                }
+            };
+            auto load_into = [&](uint4 (&dst)[MP]) {
+                if (nload < n_iter)
+                    load_stage_a16<MP>(p.xin, p.M, p.K, lb, lane, dst);
+                ++nload;
+                if (++lb == p.KB)
+                    lb = 0;
+            };
+            auto prepare = [&]() {
+                const int slot = tdone % STAGES;
+                uint8_t *st = smem + slot * SB;
+                prep_stage_a16<MP>(raw[0], p.M, lane, st + XOFF, st + SOFF, st + GOFF);
+                __syncwarp();  // orders every lane's writes before lane 0's release
+                if (lane == 0)
+                    mbar_arrive(full0 + 8 * slot);
+                ++tdone;
+#pragma unroll
+                for (int d = 0; d + 1 < PD; ++d)
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        raw[d][m] = raw[d + 1][m];
+                load_into(raw[PD - 1]);
+            };
+            const int pro = n_iter < STAGES ? n_iter : STAGES;
+            const int first = pro < 2 ? pro : 2;
+            for (int i = 0; i < first; ++i)
+                issue_w(i);
+            pdl_wait();  // x may come from the previous kernel
+#pragma unroll
+            for (int d = 0; d < PD; ++d)
+                load_into(raw[d]);
+            if (n_iter > 0)
+                prepare();
+            for (int i = first; i < pro; ++i)
+                issue_w(i);
+            issued = pro;
+            while (tdone < pro - 1)
+                prepare();
+            for (int i = pro; i < n_iter; ++i) {
+                const int slot = i % STAGES;
+                const uint32_t use = (uint32_t)(i / STAGES);
+                const bool got = W4Q_RING_WAIT(empty0 + 8 * slot, (use - 1) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0)
+                        report_error(p.err, ERR_EMPTY_WAIT);
+                    break;
+                }
+                issue_w(i);
+                issued = i + 1;
+                prepare();  // stage i - 1
+            }
+            // the last stage (after an error, every issued one, so that the
+            // drain below sees each phase complete)
+            while (tdone < issued)
+                prepare();
+        } else if (lane == 0) {
+            // --------------------- producer, activation operand from the prologue
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             const uint32_t xbytes = (uint32_t)p.M * XROW, sbytes = (uint32_t)p.M * SROW;
-            const uint32_t act_bytes = xbytes + sbytes * (MODE == W4Mode::A8 ? 2u : 1u);
+            constexpr bool COPY_G = MODE != W4Mode::A8_DOTS;  // group scales / row factors
+            const uint32_t act_bytes = xbytes + sbytes * (COPY_G ? 2u : 1u);
             auto issue_w = [&](int i, int g, int b) {
                 const int slot = i % STAGES;
                 const uint32_t bar = full0 + 8 * slot;
@@ -418,7 +660,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                          p.x + (size_t)b * p.M * (XROW / 2), xbytes, bar, pol_x);
                 bulk_g2s(smem_addr(smem + slot * SB + SOFF),
                          p.xsum + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
-                if (MODE == W4Mode::A8)
+                if (COPY_G)
                     bulk_g2s(smem_addr(smem + slot * SB + GOFF),
                              p.gscale + (size_t)b * p.M * (SROW / 4), sbytes, bar, pol_x);
             };
@@ -476,7 +718,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
         }
     } else {
         // ------------------------------------------------------ consumers
-        pdl_wait();  // act_prep's outputs (scales, counters) are read below
+        pdl_wait();  // the prologue's outputs (counters, W4A8 operand) are read below
         float acc[NB][4];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
@@ -513,8 +755,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                         const int m = nb * 8 + c2 + (e & 1);
                         const int n = tile * 16 + r + 8 * (e >> 1);
                         if (m < p.M && n < p.N)
-                            p.out[(size_t)m * p.N + n] =
-                                __float2bfloat16_rn(acc[nb][e] * p.oscale[m]);
+                            p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(acc[nb][e]);
                     }
                 return;
             }
@@ -562,7 +803,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                             v += t[q];
                 }
                 if (n < p.N)
-                    p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v * p.oscale[m]);
+                    p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
             }
         };
 
@@ -585,12 +826,12 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             if (tile < p.T)
             {
                 if constexpr (NB == 1 && MP < 8)
-                    compute_stage_packed<MP, DOTS, MODE == W4Mode::A8>(
+                    compute_stage_packed<MP, DOTS, MODE == W4Mode::A8, A16>(
                         smem_addr(smem + slot * SB + warp * TILE_BYTES),
                         smem_addr(smem + slot * SB + XOFF), smem_addr(smem + slot * SB + SOFF),
                         smem_addr(smem + slot * SB + GOFF), zrow, lane, acc, p, tile, b);
                 else
-                    compute_stage<NB, DOTS, MODE == W4Mode::A8>(
+                    compute_stage<NB, DOTS, MODE == W4Mode::A8, A16>(
                         smem_addr(smem + slot * SB + warp * TILE_BYTES),
                         smem_addr(smem + slot * SB + XOFF), smem_addr(smem + slot * SB + SOFF),
                         smem_addr(smem + slot * SB + GOFF), lane, acc, p, tile, b);
@@ -621,23 +862,30 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
     }
 }
 
-// Activation preparation (see the file comment), plus the zeroing of the
-// split-K counters.  KIND: PREP_A16 (power-of-two prescale
-// and group sums), PREP_A8 (the W4A8 quantizer).  Outputs are super-block-major:
-// xp[(k/256)*M + m][264] (16 pad bytes per row) and xsum[(g/8)*M + m][8].
-enum { PREP_A16 = 0, PREP_A8 = 2 };
-
+// The prologue (see the file comment).  Both kernels zero the split-K
+// counters after the previous kernel on the stream has finished with them;
+// act_prep also writes the activation operand, super-block-major:
+// xp[(k/256)*M + m][264] (16 pad bytes per row), xsum and gscale
+// [(g/8)*M + m][8] (W4A16: the row factor c in the row's first word).
 constexpr int PREP_THREADS = 256;
-constexpr int PREP_CHUNK = PREP_THREADS * 8;  // columns one CTA transforms
+constexpr int PREP_CHUNK = PREP_THREADS * 8;  // columns one act_prep CTA transforms
 
-// grid = (M, ceil(K / PREP_CHUNK)): every CTA finds the max over its whole
-// row (an L2-resident read of at most a few tens of KB) and transforms one
-// chunk of 2048 columns, so the prepass is one short round trip.
-template <int KIND>
+__global__ void __launch_bounds__(PREP_THREADS) splitk_reset_kernel(unsigned *__restrict__ counters,
+                                                                    int ncounters)
+{
+    pdl_launch_dependents();  // the main kernel may start streaming weights
+    pdl_wait();               // the previous kernel may still use these counters
+    for (int i = blockIdx.x * PREP_THREADS + threadIdx.x; i < ncounters; i += gridDim.x * PREP_THREADS)
+        counters[i] = 0u;
+}
+
+// grid = (M, ceil(K / PREP_CHUNK)); 8 consecutive values per thread, 4
+// consecutive threads per group of 32, one warp per 256-column super-block.
+template <bool A16>
 __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     const __nv_bfloat16 *__restrict__ x, int M, int K, __nv_bfloat16 *__restrict__ xp,
-    float *__restrict__ xsum, float *__restrict__ gscale, float *__restrict__ oscale,
-    unsigned *__restrict__ counters, int ncounters)
+    float *__restrict__ xsum, float *__restrict__ gscale, unsigned *__restrict__ counters,
+    int ncounters)
 {
     pdl_launch_dependents();  // the main kernel may start streaming weights
     pdl_wait();               // x (and this workspace) may belong to the previous kernel
@@ -648,36 +896,6 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     const int m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
     const int n8 = K / 8;
-    int sigma = 121;  // x' = value * 2^sigma on lower half-steps (2^(sigma-4) upper)
-    if (KIND == PREP_A16) {
-        // the power-of-two prescale from the row's max |x|
-        __shared__ float red[PREP_THREADS / 32];
-        float a = 0.f;
-        for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
-            const uint4 v = row[i];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                a = fmaxf(a, fmaxf(fabsf(bf16lo_to_f32(w[j])), fabsf(bf16hi_to_f32(w[j]))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if ((threadIdx.x & 31) == 0)
-            red[threadIdx.x >> 5] = a;
-        __syncthreads();
-        a = 0.f;
-#pragma unroll
-        for (int i = 0; i < PREP_THREADS / 32; ++i)
-            a = fmaxf(a, red[i]);
-        int e = 0;
-        if (a > 0.f)
-            (void)frexpf(a, &e);  // a < 2^e
-        sigma = min(max(128 - e, 6), 259);
-    }
-    if (threadIdx.x == 0 && blockIdx.y == 0)
-        oscale[m] = KIND == PREP_A8 ? 1.0f : ldexpf(1.0f, 133 - sigma);
-    // 8 consecutive values per thread; 4 consecutive threads per group of 32
     const int i = blockIdx.y * PREP_THREADS + threadIdx.x;
     const bool live = i < n8;
     float v[8];
@@ -694,22 +912,33 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
         for (int j = 0; j < 8; ++j)
             v[j] = 0.f;
     }
-    if (KIND == PREP_A8) {
-        // one scale per group of 32: sx = fp32(max |x| / 127), xq = clamp(rint(x / sx))
-        float a = 0.f;
+    float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            a = fmaxf(a, fabsf(v[j]));
+    for (int j = 0; j < 8; ++j)
+        a = fmaxf(a, fabsf(v[j]));
+    int sigma = 121;  // x' = value * 2^sigma on lower half-steps (2^(sigma-4) upper)
+    if (A16) {
+        // the power-of-two prescale from max |x| over the warp's super-block
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        int e = 0;
+        if (a > 0.f)
+            (void)frexpf(a, &e);  // a < 2^e
+        sigma = min(max(128 - e, 6), 259);
+        if (live && (i & 31) == 0)
+            gscale[((size_t)(i / 32) * M + m) * 8] = ldexpf(1.0f, 133 - sigma);
+    } else {
+        // one scale per group of 32: sx = fp32(max |x| / 127), xq = clamp(rint(x / sx))
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         const float sxg = __fdiv_rn(a, 127.0f);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxg)), -127.f), 127.f);
-        if (live && (i & 3) == 0) {
-            const int g = i / 4;  // x 2^12: the group dots come out of the MMA scaled by 2^-12
+        const int g = i / 4;  // x 2^12: the group dots come out of the MMA scaled by 2^-12
+        if (live && (i & 3) == 0)
             gscale[((size_t)(g / 8) * M + m) * 8 + (g % 8)] = sxg * 4096.0f;
-        }
     }
     float part = 0.f;
     if (live) {
@@ -733,8 +962,7 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     part += __shfl_xor_sync(0xffffffffu, part, 2);
     if (live && (i & 3) == 0) {
         const int g = i / 4;
-        xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] =
-            ldexpf(part, KIND == PREP_A8 ? -12 : sigma - 133);
+        xsum[((size_t)(g / 8) * M + m) * 8 + (g % 8)] = ldexpf(part, A16 ? sigma - 133 : -12);
     }
 }
 
@@ -856,24 +1084,25 @@ cudaError_t dispatch_main(const W4Plan &plan, const Params &p, cudaStream_t stre
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace layout: [x' bf16 (K/256)*M*264][X' f32 (K/256)*M*8]
-//                   [W4A8 group scales f32 (K/256)*M*8][out scale f32 M]
+//                   [group scales / row factors f32 (K/256)*M*8] (not for
+//                   W4A16 at MP <= 2), then
 //                   [counters u32 G*8][partials f32 P*2*M*128], 256-byte aligned.
 struct WsLayout {
-    size_t xp, xsum, gscale, oscale, counters, partial, total;
+    size_t xp, xsum, gscale, counters, partial, total;
 };
 
 WsLayout ws_layout(const W4Plan &pl, W4Mode mode)
 {
     WsLayout L;
+    // the operand the prologue prepares (W4A16 at MP <= 2: none, the main kernel does it)
+    const bool a8 = !in_kernel_prep(mode, mp_for(pl.M));
     size_t o = 0;
     L.xp = o;
-    o += align_up((size_t)pl.KB * pl.M * XROW, 256);
+    o += a8 ? align_up((size_t)pl.KB * pl.M * XROW, 256) : 0;
     L.xsum = o;
-    o += align_up((size_t)pl.KB * pl.M * SROW, 256);
+    o += a8 ? align_up((size_t)pl.KB * pl.M * SROW, 256) : 0;
     L.gscale = o;
-    o += mode == W4Mode::A8 ? align_up((size_t)pl.KB * pl.M * SROW, 256) : 0;
-    L.oscale = o;
-    o += align_up((size_t)pl.M * 4, 256);
+    o += a8 ? align_up((size_t)pl.KB * pl.M * SROW, 256) : 0;
     L.counters = o;
     o += pl.fixup ? align_up((size_t)pl.G * WARPS * 4, 256) : 0;
     L.partial = o;
@@ -967,19 +1196,14 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     p.x = reinterpret_cast<const __nv_bfloat16 *>(ws + L.xp);
     p.xsum = reinterpret_cast<const float *>(ws + L.xsum);
     p.gscale = reinterpret_cast<const float *>(ws + L.gscale);
-    p.oscale = reinterpret_cast<const float *>(ws + L.oscale);
+    p.xin = static_cast<const __nv_bfloat16 *>(x);
     p.counters = reinterpret_cast<unsigned *>(ws + L.counters);
     p.partial = reinterpret_cast<float *>(ws + L.partial);
     const int ncounters = plan.fixup ? plan.G * WARPS : 0;
-    __nv_bfloat16 *xp = reinterpret_cast<__nv_bfloat16 *>(ws + L.xp);
-    float *xsum = reinterpret_cast<float *>(ws + L.xsum);
-    float *osc = reinterpret_cast<float *>(ws + L.oscale);
     unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.counters);
-    const __nv_bfloat16 *xin = static_cast<const __nv_bfloat16 *>(x);
-    // programmatic dependent launch: the preparation launches while the
+    // programmatic dependent launch: the prologue launches while the
     // previous kernel finishes and waits for it in griddepcontrol.wait
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)plan.M, (unsigned)((plan.K + PREP_CHUNK - 1) / PREP_CHUNK));
     cfg.blockDim = dim3(PREP_THREADS);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -987,10 +1211,19 @@ cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    auto prep = mode == W4Mode::A16 ? act_prep_kernel<PREP_A16> : act_prep_kernel<PREP_A8>;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prep, xin, plan.M, plan.K, xp, xsum,
-                                       reinterpret_cast<float *>(ws + L.gscale), osc, cnt,
-                                       ncounters);
+    cudaError_t e;
+    if (in_kernel_prep(mode, mp_for(plan.M))) {
+        const int nblk = (ncounters + PREP_THREADS - 1) / PREP_THREADS;
+        cfg.gridDim = dim3((unsigned)(nblk < 1 ? 1 : (nblk > 16 ? 16 : nblk)));
+        e = cudaLaunchKernelEx(&cfg, splitk_reset_kernel, cnt, ncounters);
+    } else {
+        cfg.gridDim = dim3((unsigned)plan.M, (unsigned)((plan.K + PREP_CHUNK - 1) / PREP_CHUNK));
+        e = cudaLaunchKernelEx(&cfg, mode == W4Mode::A16 ? act_prep_kernel<true> : act_prep_kernel<false>,
+                               static_cast<const __nv_bfloat16 *>(x),
+                               plan.M, plan.K, reinterpret_cast<__nv_bfloat16 *>(ws + L.xp),
+                               reinterpret_cast<float *>(ws + L.xsum),
+                               reinterpret_cast<float *>(ws + L.gscale), cnt, ncounters);
+    }
     if (e != cudaSuccess)
         return e;
     if (mode == W4Mode::A16)

@@ -134,11 +134,12 @@ size_t w4_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int group,
 int w4_split_choice(int64_t M, int64_t N, int64_t K, int group);
 
 /* Number of kernels one w4a16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1) call
- * with these sizes launches on the current device: the activation
- * preparation (W4A8 quantizer / W4A16 power-of-two prescale or tensor-core
- * operand layout, split-K counter reset) and the main kernel; for W4A16 at
- * M >= 9 with row groups split over several CTAs, also the launch that sums
- * their fp32 partials.  -1 when the sizes are unsupported. */
+ * with these sizes launches on the current device: a prologue (split-K
+ * counter reset; W4A8: also the activation quantizer; W4A16 at M >= 9: the
+ * tensor-core operand layout) and the main kernel (W4A16 at M <= 8 prepares
+ * its activation operand itself); for W4A16 at M >= 9 with row groups split
+ * over several CTAs, also the launch that sums their fp32 partials.  -1 when
+ * the sizes are unsupported. */
 int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
 
 /* out = x . dequant(packed)^T, W4A16.

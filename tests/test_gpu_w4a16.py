@@ -109,7 +109,8 @@ def test_workspace_too_small_is_rejected(cuda):
     with pytest.raises(w4q.W4QError) as e:
         w4q.w4a8_gemm(x, packed, N, K, workspace=small, out=out)
     assert e.value.status == 4
-    # W4A16 always needs the prepared activation operand: 16 bytes is short
+    # W4A16 at this shape splits row groups over CTAs: its split-K counters
+    # and partials do not fit in 16 bytes
     with pytest.raises(w4q.W4QError) as e:
         w4q.w4a16_gemm(x, packed, N, K, workspace=small[:16], out=out)
     assert e.value.status == 4
