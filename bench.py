@@ -50,8 +50,11 @@ MEASURED_TRAFFIC = {
         164167424, ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh"),
         "3371cdcb57ff755b63f3836d7e7f4d5abc2b54778bad25027408690b8423977a"),
     "w4a16 N=39936 K=6656 M=4": (
-        161181440, ("gemv_w4.cu", "common.cuh"),
-        "8cbca7a8a80cf0b433f9304d390324387197f699584d1e23ada76f2ee2ee550a"),
+        160975360, ("gemv_w4.cu", "common.cuh"),
+        "866d52881d0c3833e67bd0909e0090de3d78195182207473b37eee1d122071bd"),
+    "w4a16 N=39936 K=6656 M=1": (
+        161075712, ("gemv_w4.cu", "common.cuh"),
+        "866d52881d0c3833e67bd0909e0090de3d78195182207473b37eee1d122071bd"),
 }
 
 
