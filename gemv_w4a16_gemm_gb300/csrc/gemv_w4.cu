@@ -785,25 +785,43 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 return;
             const int slot0 = (range_begin(p, cf) == gb) ? 0 : 1;
             const int nc = cl - cf + 1;
-            for (int i = lane; i < p.M * 16; i += 32) {
-                const int m = i / 16, row = i % 16;
-                const int n = tile * 16 + row;
-                const size_t off = (size_t)m * GROUP_ROWS + warp * 16 + row;
-                const float *first = p.partial + (size_t)(cf * 2 + slot0) * seg + off;
-                const float *rest = p.partial + (size_t)(cf * 2 + 2) * seg + off;  // slot 0 of cf+1..
-                float v = __ldcg(first);
-                for (int j = 0; j + 1 < nc; j += 8) {  // eight independent loads, then an in-order sum
-                    float t[8];
+            // this lane's outputs i = lane + 32 k (M * 16 of them per row tile);
+            // the loads of all of them go out together, eight contributors at
+            // a time, and each output is summed in CTA order
+            constexpr int MMAX = NB == 1 ? MP : NB * 8;  // M <= MMAX
+            constexpr int NV = MMAX * 16 / 32 > 0 ? MMAX * 16 / 32 : 1;
+            const float *first[NV], *rest[NV];
+            bool live[NV];
+            float v[NV];
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int i = lane + 32 * k, m = i / 16, row = i % 16;
+                live[k] = i < p.M * 16;
+                const size_t off = (size_t)(live[k] ? m : 0) * GROUP_ROWS + warp * 16 + row;
+                first[k] = p.partial + (size_t)(cf * 2 + slot0) * seg + off;
+                rest[k] = p.partial + (size_t)(cf * 2 + 2) * seg + off;  // slot 0 of cf+1..
+                v[k] = live[k] ? __ldcg(first[k]) : 0.f;
+            }
+            for (int j = 0; j + 1 < nc; j += 8) {
+                float t[NV][8];
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        t[q] = (j + q + 1 < nc) ? __ldcg(rest + (size_t)(j + q) * 2 * seg) : 0.f;
+                        t[k][q] = (live[k] && j + q + 1 < nc)
+                                      ? __ldcg(rest[k] + (size_t)(j + q) * 2 * seg) : 0.f;
+#pragma unroll
+                for (int k = 0; k < NV; ++k)
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         if (j + q + 1 < nc)
-                            v += t[q];
-                }
-                if (n < p.N)
-                    p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
+                            v[k] += t[k][q];
+            }
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int i = lane + 32 * k, m = i / 16, n = tile * 16 + i % 16;
+                if (live[k] && n < p.N)
+                    p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v[k]);
             }
         };
 
