@@ -50,11 +50,11 @@ MEASURED_TRAFFIC = {
         164167424, ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh"),
         "3371cdcb57ff755b63f3836d7e7f4d5abc2b54778bad25027408690b8423977a"),
     "w4a16 N=39936 K=6656 M=4": (
-        160975360, ("gemv_w4.cu", "common.cuh"),
-        "866d52881d0c3833e67bd0909e0090de3d78195182207473b37eee1d122071bd"),
+        161165312, ("gemv_w4.cu", "common.cuh"),
+        "94790c720b04260d76c714338e8ac58b9146ad9f904a90691b0297456cab728b"),
     "w4a16 N=39936 K=6656 M=1": (
-        161075712, ("gemv_w4.cu", "common.cuh"),
-        "866d52881d0c3833e67bd0909e0090de3d78195182207473b37eee1d122071bd"),
+        160952320, ("gemv_w4.cu", "common.cuh"),
+        "94790c720b04260d76c714338e8ac58b9146ad9f904a90691b0297456cab728b"),
 }
 
 

@@ -136,3 +136,50 @@ def test_zero_activation_gives_zero(cuda):
         out = w4q.w4a16_gemm(torch.zeros(M, K, dtype=torch.bfloat16, device=cuda), packed, N, K)
         assert torch.all(out == 0)
     assert w4q.device_error() == 0
+
+
+def _magnitude_rows(K, seed=11):
+    """Nine bf16 activation rows of very different magnitudes (K = 8 super-blocks
+    of 256): ordinary, near the bf16 normal limit, 2^100, 2^-100, one lone tiny
+    super-block, alternating zero / 2^40 super-blocks, 2^-60 .. 2^80 across the
+    row, subnormals only, and zero.  Every value stays below 2^122."""
+    g = torch.Generator().manual_seed(seed)
+    r = lambda: torch.randn(K, generator=g)  # noqa: E731
+    rows = [r(), r() * 2.0 ** -126, r() * 2.0 ** 100, r() * 2.0 ** -100]
+    lone = torch.zeros(K)
+    lone[768:1024] = r()[768:1024] * 2.0 ** -60
+    alt = r() * 2.0 ** 40
+    for b in range(0, K // 256, 2):
+        alt[256 * b:256 * (b + 1)] = 0
+    wide = r()
+    for b in range(K // 256):
+        wide[256 * b:256 * (b + 1)] *= 2.0 ** (-60 + 20 * b)
+    rows += [lone, alt, wide, r() * 2.0 ** -131, torch.zeros(K)]
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+def test_activation_magnitudes_per_row(cuda):
+    # The power-of-two prescale of x is chosen per row and 256-column
+    # super-block (in the main kernel at M <= 2, in the prologue above), so
+    # every row must come out right relative to its own size.  Per row:
+    # |out - ref| <= 1e-2 * max |ref| + 2^-133 (one bf16 subnormal step, the
+    # output format's own resolution); zero rows give exact zeros.
+    N, K = 384, 2048
+    W, q, s, z = quantized(N, K, seed=7)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    X = _magnitude_rows(K)
+    for M in (1, 2, 3, 4, 8):
+        for start in range(0, X.shape[0], M):
+            idx = [(start + j) % X.shape[0] for j in range(M)]
+            x = X[idx]
+            out = w4q.w4a16_gemm(x.to(cuda), packed, N, K).double().cpu().numpy()
+            ref = oracle.w4a16(x, q, s, z)
+            for j, row in enumerate(idx):
+                what = "M=%d row regime %d" % (M, row)
+                assert (abs(out[j]) < float("inf")).all(), what
+                if not x[j].any():
+                    assert (out[j] == 0).all(), what
+                    continue
+                err = abs(out[j] - ref[j]).max()
+                assert err <= 1e-2 * abs(ref[j]).max() + 2.0 ** -133, (what, err, abs(ref[j]).max())
+    assert w4q.device_error() == 0
