@@ -1156,6 +1156,12 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     const long long U = (long long)groups * pl.KB;
     if (mode == W4Mode::A8_DOTS)
         split = 1;  // every unit is processed once; no accumulation across CTAs
+    // Tensor-core path with few super-blocks and no more row-group pairs than
+    // SMs: each CTA takes a pair's whole K.  The partial-sum launch a split
+    // would need costs more than the CTA's extra stages (1536 x 512, M = 16:
+    // 7.1 -> 4.8 us).
+    if (split < 0 && pl.umma && pl.KB <= 4 && pl.G2 <= (sm_count > 0 ? sm_count : 1))
+        split = 1;
     if (split < 0)
         split = 0;
     if (split >= 1) {

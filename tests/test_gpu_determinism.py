@@ -21,7 +21,9 @@ def test_graph_replay_matches_eager(cuda, M):
     xa8 = x[: min(M, 8)].contiguous()          # W4A8 serves up to 8 rows
     eager = (w4q.w4a16_gemm(x, packed, N, K), w4q.w4a8_gemm(xa8, packed, N, K),
              w4q.w8_gemv(x8, W8, sc))
-    ws = torch.empty(max(w4q.workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=cuda)
+    # one workspace for the W4A16 call (M rows) and the W4A8 call (min(M, 8) rows)
+    need = max(w4q.workspace_bytes(M, N, K), w4q.workspace_bytes(min(M, 8), N, K), 16)
+    ws = torch.empty(need, dtype=torch.uint8, device=cuda)
     outs = (torch.empty_like(eager[0]), torch.empty_like(eager[1]), torch.empty_like(eager[2]))
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
