@@ -65,6 +65,8 @@
 //         no waiting on other CTAs) and writes the outputs.
 //       * Every wait is bounded (one second of %globaltimer); on expiry the
 //         kernel sets a bit in the error word, drains its copies and returns.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -1067,10 +1069,20 @@ template <int NB, W4Mode MODE, int MP>
 cudaError_t launch_main(const Params &p, cudaStream_t stream)
 {
     auto fn = w4_kernel<NB, MODE, MP>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_for<NB, MODE>());
+    // the dynamic shared-memory opt-in, once per device (a bit per device)
+    static std::atomic<unsigned long long> opted_in{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit == 0 || !(opted_in.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_for<NB, MODE>());
+        if (e != cudaSuccess)
+            return e;
+        opted_in.fetch_or(bit, std::memory_order_release);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.P);
     cfg.blockDim = dim3(THREADS);

@@ -59,6 +59,8 @@ class W4QError(RuntimeError):
 def lib():
     """The loaded libw4q.so; raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -117,8 +119,9 @@ def kernel_launches(M: int, N: int, K: int, w4a8: bool = False, group: int = GRO
 
 
 def _workspace(M, N, K, group, split_k, workspace, device):
-    need = workspace_bytes(M, N, K, group, split_k)
+    # a given workspace is passed as is (the library checks its size)
     if workspace is None:
+        need = workspace_bytes(M, N, K, group, split_k)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
     return workspace, workspace.numel() * workspace.element_size()
 
