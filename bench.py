@@ -51,10 +51,10 @@ MEASURED_TRAFFIC = {
         "3371cdcb57ff755b63f3836d7e7f4d5abc2b54778bad25027408690b8423977a"),
     "w4a16 N=39936 K=6656 M=4": (
         161165312, ("gemv_w4.cu", "common.cuh"),
-        "80f1af299eea18e413bad0fd86e03446c7a6812e2b5adb360a7161562d9ce2e9"),
+        "9647256fcdca3d2bf23a793c0c2494e1fc782aefd68a5d53469b4e69cd1288e9"),
     "w4a16 N=39936 K=6656 M=1": (
         160952320, ("gemv_w4.cu", "common.cuh"),
-        "80f1af299eea18e413bad0fd86e03446c7a6812e2b5adb360a7161562d9ce2e9"),
+        "9647256fcdca3d2bf23a793c0c2494e1fc782aefd68a5d53469b4e69cd1288e9"),
 }
 
 
