@@ -8,7 +8,7 @@
 // must not pause in an allocator or fragment the heap); and plug-ins running
 // inside a framework whose device memory belongs to the framework's own
 // pool.  For them this file keeps the scratch memory the W4A16 kernels need
-// (prepared activations, group sums, output scales, split-K counters and
+// (prepared activations, group sums, row factors, split-K counters and
 // partial sums) in one fixed array in device memory that belongs to the
 // library.  The kernels and the arithmetic are exactly those of w4a16_gemm;
 // only the source of the scratch differs.
