@@ -162,8 +162,11 @@ int w4a16_gemm(const void *x_bf16, const void *packed, void *out_bf16,
  * 16*8-row tile group's K range into s contiguous parts of whole 256-wide
  * super-blocks (legal iff s <= K/256, "test_int4_quantized_gemm.py",
  * Int4QuantizedGemmRulesTest: one 256-wide K tile per split), partials are
- * summed in fixed order; split_k = 0 is the balanced stream-K partition the
- * library uses by default.  Illegal s returns W4Q_ERR_UNSUPPORTED. */
+ * summed in fixed order; split_k = 0 is the balanced stream-K partition.
+ * The library's own choice (w4a16_gemm, see w4_split_choice) is stream-K,
+ * except on the tensor-core path (M >= 9) with at most 4 super-blocks and
+ * no more 256-row pairs than SMs, where it is 1 (whole K per CTA, no
+ * partial-sum launch).  Illegal s returns W4Q_ERR_UNSUPPORTED. */
 int w4a16_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
                      int64_t M, int64_t N, int64_t K, int group, int split_k,
                      void *workspace, size_t workspace_bytes, void *stream);

@@ -183,3 +183,20 @@ def test_activation_magnitudes_per_row(cuda):
                 err = abs(out[j] - ref[j]).max()
                 assert err <= 1e-2 * abs(ref[j]).max() + 2.0 ** -133, (what, err, abs(ref[j]).max())
     assert w4q.device_error() == 0
+
+
+def test_partition_choice_and_launch_count(cuda):
+    # Tensor-core path (M >= 9) with at most 4 super-blocks and no more
+    # 256-row pairs than SMs: each CTA takes a pair's whole K (split 1), so
+    # the call is two launches, with no partial-sum launch.
+    for M in (9, 16, 64):
+        assert w4q.split_choice(M, 1536, 512) == 1, M
+        assert w4q.kernel_launches(M, 1536, 512) == 2, M
+    # Longer K keeps the balanced stream-K partition, and its partial-sum
+    # launch where row-group pairs are split over CTAs.
+    assert w4q.split_choice(16, 39936, 6656) == 0
+    assert w4q.kernel_launches(16, 39936, 6656) == 3
+    # The mma.sync path (M <= 8) keeps stream-K with few super-blocks too
+    # (its split-K sum is inside the main kernel).
+    assert w4q.split_choice(4, 1536, 512) == 0
+    assert w4q.kernel_launches(4, 1536, 512) == 2
