@@ -12,7 +12,11 @@ header for the readings taken where the pages are silent):
   (INT4, group 32 along K, asymmetric min-max).
 * w4a16 -- "test_int4_quantized_gemm.py", the dequant + F.linear reference.
 * act_quant / w4a8_group_dots / w4a8 -- "test_int4_quantized_gemm.py",
-  W4A8 bucket kernels and Int4QuantizedGemmPrecisionTest.
+  W4A8 bucket kernels and Int4QuantizedGemmPrecisionTest (one activation
+  scale per (row, group of 32)).
+* act_quant_row / w4a8_row -- the same W4A8 with one activation scale per
+  whole row (scale = absmax / 127), the scheme of the 39936 x 6656 W4A8
+  workload.
 * w8 -- "gpt-fast issue #114", WeightOnlyInt8Linear.forward.
 * pack_w4 / unpack_w4 -- this library's packed layout (no page counterpart).
 """
@@ -69,6 +73,8 @@ def _load():
                 "oracle_act_quant": [P, I, I, P, P],
                 "oracle_w4a8_group_dots": [P, P, P, I, I, I, P],
                 "oracle_w4a8": [P, P, P, P, P, I, I, I, I, I, P],
+                "oracle_act_quant_row": [P, I, I, P, P],
+                "oracle_w4a8_row": [P, P, P, P, P, I, I, I, I, I, P],
                 "oracle_w8": [P, P, P, I, I, I, I, I, P],
                 "oracle_set_threads": [ctypes.c_int],
             }
@@ -160,6 +166,17 @@ def act_quant(x_bf16, K: int):
     return xq, sx
 
 
+def act_quant_row(x_bf16, K: int):
+    """Symmetric int8 activations, one scale per whole row:
+    (xq i8 [M,K], sx f32 [M])."""
+    x = _u16(x_bf16).reshape(-1, K)
+    M = x.shape[0]
+    xq = np.empty((M, K), np.int8)
+    sx = np.empty((M,), np.float32)
+    _load().oracle_act_quant_row(_ptr(x), M, K, _ptr(xq), _ptr(sx))
+    return xq, sx
+
+
 def w4a8_group_dots(xq, q, z) -> np.ndarray:
     N, K = q.shape
     M = xq.shape[0]
@@ -177,6 +194,18 @@ def w4a8(xq, sx, q, s, z, n0: int = 0, n1: int | None = None) -> np.ndarray:
     _load().oracle_w4a8(_ptr(np.ascontiguousarray(xq)),
                         _ptr(np.ascontiguousarray(sx, dtype=np.float32)),
                         _ptr(q), _ptr(s), _ptr(z), M, N, K, n0, n1, _ptr(out))
+    return out
+
+
+def w4a8_row(xq, sx, q, s, z, n0: int = 0, n1: int | None = None) -> np.ndarray:
+    """fp64 out[M, n1-n0] = sx[m] * sum_g s * D for per-row int8 activations."""
+    N, K = q.shape
+    M = xq.shape[0]
+    n1 = N if n1 is None else n1
+    out = np.empty((M, n1 - n0), np.float64)
+    _load().oracle_w4a8_row(_ptr(np.ascontiguousarray(xq)),
+                            _ptr(np.ascontiguousarray(sx, dtype=np.float32).reshape(M)),
+                            _ptr(q), _ptr(s), _ptr(z), M, N, K, n0, n1, _ptr(out))
     return out
 
 

@@ -34,6 +34,11 @@
  *    0, 15), both from the STORED bf16 s, rint = round half to even;
  *  - dequant(q) = (q - z) * s.
  *
+ * W4A8 comes in two activation granularities: one int8 scale per whole row
+ * (oracle_act_quant_row / oracle_w4a8_row, the 39936 x 6656 W4A8
+ * workload's scheme) and one per (row, group of 32) (oracle_act_quant /
+ * oracle_w4a8, the finer variant that passes the pages' outlier case).
+ *
  * parity pins: see the oracle tests (exact-rational brute force, invariants,
  * one-hot and all-ones special cases, library matmul cross-check).
  */
@@ -336,6 +341,42 @@ void oracle_act_quant(const uint16_t *x, int64_t M, int64_t K, int8_t *xq,
         }
 }
 
+/* The per-row variant: one symmetric int8 scale for each whole activation
+ * row, the scheme of the 39936 x 6656 W4A8 workload ("per-row symmetric
+ * int8 (scale=absmax/127)").  Per row m, in IEEE fp32 (round to nearest
+ * even):
+ *   a = max_k |x[m,k]|,  sx[m] = a / 127,
+ *   xq[m,k] = clamp(rint(x[m,k] / sx[m]), -127, 127),  xq = 0 when a == 0.
+ * The same fp32 decision rule as oracle_act_quant, over the row instead of
+ * the group.  sx: f32 [M]. */
+void oracle_act_quant_row(const uint16_t *x, int64_t M, int64_t K, int8_t *xq,
+                          float *sx)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        float a = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float v = fabsf(bf16_to_float(x[m * K + k]));
+            if (v > a)
+                a = v;
+        }
+        volatile float sxm = a / 127.0f;
+        sx[m] = sxm;
+        for (int64_t k = 0; k < K; ++k) {
+            if (a == 0.0f) {
+                xq[m * K + k] = 0;
+                continue;
+            }
+            volatile float t = bf16_to_float(x[m * K + k]) / sxm;
+            float r = rintf(t);
+            if (r > 127.0f)
+                r = 127.0f;
+            if (r < -127.0f)
+                r = -127.0f;
+            xq[m * K + k] = (int8_t)r;
+        }
+    }
+}
+
 /* D[m][n][g] = sum_{k in group g} (q[n,k] - z[n,g]) * xq[m,k], exact int. */
 void oracle_w4a8_group_dots(const int8_t *xq, const uint8_t *q,
                             const uint8_t *z, int64_t M, int64_t N, int64_t K,
@@ -377,6 +418,32 @@ void oracle_w4a8(const int8_t *xq, const float *sx, const uint8_t *q,
                 acc += (double)sx[m * G + g] * bf16_to_double(s[n * G + g]) * (double)d;
             }
             out[m * W + (n - n0)] = acc;
+        }
+}
+
+/* Per-row W4A8: out[m, n - n0] = sx[m] * sum_g s[n,g] * D[m][n][g] in
+ * fp64, with D the exact integer group dots and sx: f32 [M] from
+ * oracle_act_quant_row. */
+void oracle_w4a8_row(const int8_t *xq, const float *sx, const uint8_t *q,
+                     const uint16_t *s, const uint8_t *z, int64_t M, int64_t N,
+                     int64_t K, int64_t n0, int64_t n1, double *out)
+{
+    (void)N;
+    int64_t G = K / GROUP, W = n1 - n0;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = n0; n < n1; ++n)
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t g = 0; g < G; ++g) {
+                int64_t d = 0;
+                for (int64_t i = 0; i < GROUP; ++i) {
+                    int64_t k = g * GROUP + i;
+                    d += ((int64_t)q[n * K + k] - (int64_t)z[n * G + g]) *
+                         (int64_t)xq[m * K + k];
+                }
+                acc += bf16_to_double(s[n * G + g]) * (double)d;
+            }
+            out[m * W + (n - n0)] = (double)sx[m] * acc;
         }
 }
 

@@ -467,6 +467,125 @@ def test_w4a8_outlier_precision_criteria():
 
 
 # --------------------------------------------------------------------------
+# W4A8 with one activation scale per whole row (scale = absmax / 127)
+# --------------------------------------------------------------------------
+
+
+def test_act_quant_row_hand_derived():
+    # one scale for the whole row: the row maximum 127 (in group 1) gives
+    # sx = 1 exactly, so group 0's values round on their own
+    # (0.5 -> 0, 1.5 -> 2, 2.5 -> 2: half to even) and a group of small
+    # values is flattened to zero; max 254 gives sx = 2 (x / 2 = .5 ties);
+    # an all-zero row gives sx = 0 and codes 0.
+    K = 96
+    r0 = ([0.5, 1.5, 2.5, -0.5, -1.5, 3.0, 0.0, -3.5] + [0.0] * 24
+          + [127.0, -127.0] + [0.0] * 30
+          + [0.25, -0.25, 0.375, 0.5] + [0.0] * 28)
+    r1 = [254.0, 1.0, 3.0, -1.0, 5.0, 0.0, -254.0, 2.0] + [0.0] * 88
+    r2 = [0.0] * K
+    x = np.array([[float_to_bits(v) for v in r] for r in (r0, r1, r2)], np.uint16)
+    xq, sx = oracle.act_quant_row(x, K)
+    assert sx.shape == (3,) and sx.tolist() == [1.0, 2.0, 0.0]
+    assert list(xq[0, :8]) == [0, 2, 2, 0, -2, 3, 0, -4]
+    assert list(xq[0, 32:34]) == [127, -127]
+    assert list(xq[0, 64:68]) == [0, 0, 0, 0]           # |v| <= 0.5 at sx = 1
+    assert list(xq[1, :8]) == [127, 0, 2, 0, 2, 0, -127, 1]
+    assert not xq[2].any()
+
+
+def test_act_quant_row_matches_exact_rounding_away_from_ties():
+    M, K = 3, 4096
+    x = randn_bits((M, K), 151)
+    xq, sx = oracle.act_quant_row(x, K)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(xf).max(axis=1)
+    assert np.array_equal(sx, (amax / np.float32(127)).astype(np.float32))
+    near = 0
+    for m in range(M):
+        for k in range(0, K, 5):
+            v = Fraction(float(xf[m, k])) / Fraction(float(sx[m]))
+            if abs(abs(v - int(v)) - Fraction(1, 2)) < Fraction(1, 2 ** 16):
+                near += 1
+                continue
+            assert xq[m, k] == max(-127, min(127, round(v)))
+    assert near < 16
+    assert (np.abs(xq).max(axis=1) == 127).all()        # every row reaches its maximum code
+
+
+def test_act_quant_row_one_large_value_rescales_the_whole_row():
+    # the opposite of the per-group rule: a large value anywhere changes the
+    # scale, and so the codes, of every group of its row
+    K = 96
+    base = randn_bits((1, K), 152)[0]
+    big = base.copy()
+    big[40] = float_to_bits(500.0)
+    xq, sx = oracle.act_quant_row(np.stack([base, big]), K)
+    assert sx[1] > 50 * sx[0]
+    assert not np.array_equal(xq[0, :32], xq[1, :32])
+    assert not np.array_equal(xq[0, 64:], xq[1, 64:])
+
+
+def test_act_quant_row_equals_per_group_when_every_group_has_the_row_max():
+    # where every group of 32 holds the row's max |x|, the per-group scales all
+    # equal the row scale, so both rules give the same scale and codes
+    M, K = 2, 512
+    x = randn_bits((M, K), 153)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    top = float(np.abs(xf).max()) * 2
+    for m in range(M):
+        for g in range(K // 32):
+            x[m, 32 * g + (g * 7 + m) % 32] = float_to_bits(top if g % 2 else -top)
+    xq_r, sx_r = oracle.act_quant_row(x, K)
+    xq_g, sx_g = oracle.act_quant(x, K)
+    assert np.array_equal(np.repeat(sx_r[:, None], K // 32, axis=1), sx_g)
+    assert np.array_equal(xq_r, xq_g)
+
+
+def test_w4a8_row_reduces_to_w4a16_on_integer_activations():
+    # integer rows that reach 127: sx = 1 and xq = x, so per-row W4A8 is W4A16
+    N, K, M = 64, 768, 3
+    _, q, s, z = _quantized(N, K, 154)
+    rng = np.random.default_rng(155)
+    xi = rng.integers(-126, 127, (M, K))
+    xi[:, 17] = 127
+    x = np.array([[float_to_bits(float(v)) for v in row] for row in xi], np.uint16)
+    xq, sx = oracle.act_quant_row(x, K)
+    assert np.all(sx == 1.0) and np.array_equal(xq, xi)
+    np.testing.assert_allclose(oracle.w4a8_row(xq, sx, q, s, z), oracle.w4a16(x, q, s, z),
+                               rtol=1e-13, atol=1e-9)
+
+
+def test_w4a8_row_combination_is_the_row_scale_times_the_scaled_group_dots():
+    # out[m, n] = sx[m] * sum_g s[n, g] * D[m, n, g], D from an int64 einsum
+    N, K, M = 40, 512, 4
+    _, q, s, z = _quantized(N, K, 156)
+    x = randn_bits((M, K), 157)
+    xq, sx = oracle.act_quant_row(x, K)
+    qq = q.reshape(N, K // 32, 32).astype(np.int64) - z[:, :, None]
+    D = np.einsum("ngi,mgi->mng", qq, xq.reshape(M, K // 32, 32).astype(np.int64))
+    sf = np.vectorize(bits_to_float)(s).astype(np.float64)
+    ref = sx.astype(np.float64)[:, None] * np.einsum("ng,mng->mn", sf, D.astype(np.float64))
+    np.testing.assert_allclose(oracle.w4a8_row(xq, sx, q, s, z), ref, rtol=1e-12, atol=1e-12)
+    # and the per-group combination with the row scale broadcast to every group
+    sxg = np.repeat(sx[:, None], K // 32, axis=1)
+    np.testing.assert_allclose(oracle.w4a8(xq, sxg, q, s, z), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_w4a8_row_precision_class_against_w4a16_gaussian():
+    # "test_int4_quantized_gemm.py", Int4QuantizedGemmPrecisionTest: on
+    # gaussian activations mean |a8 - a16| / mean |a16| <= 0.02 (one scale
+    # per row suffices there; the outlier case needs the per-group rule).
+    N, K = 512, 6656
+    _, q, s, z = _quantized(N, K, 158)
+    for M in (1, 4):
+        x = randn_bits((M, K), 159 + M)
+        xq, sx = oracle.act_quant_row(x, K)
+        a8 = oracle.w4a8_row(xq, sx, q, s, z)
+        a16 = oracle.w4a16(x, q, s, z)
+        assert np.abs(a8 - a16).mean() / np.abs(a16).mean() < 0.02
+
+
+# --------------------------------------------------------------------------
 # W8
 # --------------------------------------------------------------------------
 
