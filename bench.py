@@ -5,8 +5,10 @@ entry point once per (shape, M), each call on its own copy of the packed
 weights so that every call streams its weights from HBM:
 
   * W8 GEMV 8192 x 8192, M = 1                       ("gpt-fast issue #114")
+  * W4A16 (256,768), M = 1 (the tiny case)
   * W4A16 (8448,6656) (6656,4096) (6656,19968) (256,6656), M = 1..4
-  * W4A8  (39936,6656), M = 1..4
+  * W4A8  (39936,6656), M = 1..4, one activation scale per row, and the
+    same with one per (row, group of 32)
   * W4A16 (39936,6656) (6656,19968) (1536,512), M = 16, 64
     ("test_int4_quantized_gemm.py": MODEL_SHAPES, SMALL_SHAPES, buckets)
 
@@ -15,7 +17,7 @@ of the step must read) / step time; the JSON line also carries each call's
 microseconds, GB/s and fraction of the measured HBM copy bandwidth.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-    python bench.py --summarize-ncu gpurun_out/launches.csv   # launch-list shares
+    python bench.py --summarize-ncu LAUNCHES.csv   # launch-list shares of an ncu --csv log
 """
 from __future__ import annotations
 
@@ -76,14 +78,17 @@ PAGES_W8_GBS = 1277.19   # "gpt-fast issue #114": compiled int8 GEMV, 8192^2, M=
 # ----------------------------------------------------------------- workload
 
 def step_calls():
-    """(kind, N, K, M) of one step, in launch order."""
-    calls = [("w8", workloads.W8_GEMV["N"], workloads.W8_GEMV["K"], 1)]
+    """(kind, N, K, M) of one step, in launch order.  Kinds: w8, w4a16, w4a8r
+    (W4A8, one activation scale per row), w4a8 (one per group of 32)."""
+    calls = [("w8", workloads.W8_GEMV["N"], workloads.W8_GEMV["K"], 1),
+             ("w4a16", workloads.TINY_W4A16["N"], workloads.TINY_W4A16["K"], 1)]
     for (N, K) in workloads.W4A16_GEMV_SHAPES:
         for M in workloads.W4A16_GEMV_MS:
             calls.append(("w4a16", N, K, M))
     N, K = workloads.W4A8_SHAPE
-    for M in workloads.W4A8_MS:
-        calls.append(("w4a8", N, K, M))
+    for kind in ("w4a8r", "w4a8"):
+        for M in workloads.W4A8_MS:
+            calls.append((kind, N, K, M))
     for (N, K) in workloads.TC_SHAPES:
         for M in workloads.TC_MS:
             calls.append(("w4a16", N, K, M))
@@ -112,7 +117,7 @@ def kernel_name(kind, M):
     if kind == "w4a16" and M >= 9:
         return "w4_umma_kernel<NP=%d>" % ((M + 15) // 16 * 16)
     nb = 1 if M <= 8 else (2 if M <= 16 else (4 if M <= 32 else 8))
-    return "w4_kernel<NB=%d,%s>" % (nb, "A8" if kind == "w4a8" else "A16")
+    return "w4_kernel<NB=%d,%s>" % (nb, "A16" if kind == "w4a16" else "A8")
 
 
 # ------------------------------------------------------------------- clocks
@@ -198,7 +203,8 @@ class Suite:
         self.ws = {}
         users = {}
         for kind, N, K, M in self.calls:
-            users[(kind, N, K)] = users.get((kind, N, K), 0) + 1
+            key = self.wkey(kind, N, K)
+            users[key] = users.get(key, 0) + 1
         for key, n_users in users.items():
             kind, N, K = key
             per = weight_bytes(kind, N, K)
@@ -224,29 +230,37 @@ class Suite:
                 self.ws[i] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
+    @staticmethod
+    def wkey(kind, N, K):
+        """The weight pool a call reads (every W4 kind shares the packed format)."""
+        return ("w8" if kind == "w8" else "w4", N, K)
+
     def launch(self, i, copy_index, x=None, out=None):
         kind, N, K, M = self.calls[i]
-        pool = self.pools[(kind, N, K)]
+        pool = self.pools[self.wkey(kind, N, K)]
         w = pool[copy_index % len(pool)]
         x = self.x[i] if x is None else x
         out = self.out[i] if out is None else out
         if kind == "w8":
-            self.w4q.w8_gemv(x, w, self.extra[(kind, N, K)], out=out)
+            self.w4q.w8_gemv(x, w, self.extra[self.wkey(kind, N, K)], out=out)
         elif kind == "w4a16":
             self.w4q.w4a16_gemm(x, w, N, K, out=out, workspace=self.ws[i])
+        elif kind == "w4a8r":
+            self.w4q.w4a8_gemm_rowscale(x, w, N, K, out=out, workspace=self.ws[i])
         else:
             self.w4q.w4a8_gemm(x, w, N, K, out=out, workspace=self.ws[i])
 
     def launches_per_step(self):
         n = 0
         for kind, N, K, M in self.calls:
-            n += 1 if kind == "w8" else self.w4q.kernel_launches(M, N, K, kind == "w4a8")
+            n += 1 if kind == "w8" else self.w4q.kernel_launches(M, N, K, kind != "w4a16")
         return n
 
     def step_copy_index(self, i):
         """Distinct copy per call within a step (calls of one shape rotate)."""
         kind, N, K, M = self.calls[i]
-        same = [j for j, c in enumerate(self.calls[:i]) if c[:3] == (kind, N, K)]
+        key = self.wkey(kind, N, K)
+        same = [j for j, c in enumerate(self.calls[:i]) if self.wkey(*c[:3]) == key]
         return len(same)
 
 
@@ -270,7 +284,7 @@ def measure_calls(suite, reps=3):
     torch = suite.torch
     res = []
     for i, (kind, N, K, M) in enumerate(suite.calls):
-        pool = suite.pools[(kind, N, K)]
+        pool = suite.pools[suite.wkey(kind, N, K)]
         R = max(50, len(pool))
         g = _graph(torch, lambda: [suite.launch(i, r) for r in range(R)])
         times = []
@@ -396,15 +410,21 @@ def run_gpu(args, rank, world, dist):
     by_kernel = {}
     for c in per_call:
         by_kernel[c["kernel"]] = by_kernel.get(c["kernel"], 0.0) + c["share"]
+    roofline = dominant_kernel_roofline(per_call, peaks, args.traffic)
     dom = max(per_call, key=lambda c: c["share"])
     dom_alg = algorithmic_bytes(dom["kind"], dom["N"], dom["K"], dom["M"])
     achieved = dom_alg / dom["us"] / 1e3
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": (args.traffic if args.traffic is not None else measured_traffic(dom["call"])),
-                "kernel": dom["kernel"], "call": dom["call"],
-                "algorithmic_bytes_per_launch": dom_alg, "us_per_launch": round(dom["us"], 3),
-                "peak_source": peaks["source"]}
+    roofline_call = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": measured_traffic(dom["call"]), "kernel": dom["kernel"],
+                     "call": dom["call"], "algorithmic_bytes_per_launch": dom_alg,
+                     "us_per_launch": round(dom["us"], 3), "peak_source": peaks["source"]}
+    tensor = [{"call": c["call"], "kernel": c["kernel"],
+               "achieved": round(2.0 * c["M"] * c["N"] * c["K"] / c["us"] / 1e6, 1),
+               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+               "frac": round(2.0 * c["M"] * c["N"] * c["K"] / c["us"] / 1e6 / peaks["bf16_tflops"], 4),
+               "peak_source": peaks["source"].replace("copy", "cuBLAS bf16 GEMM, burst")}
+              for c in per_call if c["kind"] == "w4a16" and c["M"] >= 9]
     value = replica_value(world, step_weight, ms)
     w8 = next(c for c in per_call if c["kind"] == "w8")
     clocks = clk.summary()
@@ -419,6 +439,8 @@ def run_gpu(args, rank, world, dist):
                          "the step streams %.2f GB" % (step_weight / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roofline,
+        "roofline_largest_call": roofline_call,
+        "tensor_roofline": tensor,
         "e2e": {"value": round(world * step_weight / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -439,6 +461,37 @@ def run_gpu(args, rank, world, dist):
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+def dominant_kernel_roofline(per_call, peaks, traffic_override=None):
+    """Roofline of the kernel with the largest share of the step, over all its
+    calls: algorithmic bytes per launch (their mean) over its mean launch
+    duration (each call's per-launch CUDA-event time), against the measured
+    copy bandwidth; traffic = ncu DRAM bytes per launch when every one of its
+    calls has a current figure, else null."""
+    kern = {}
+    for c in per_call:
+        k = kern.setdefault(c["kernel"], {"share": 0.0, "bytes": 0, "us": 0.0, "calls": []})
+        k["share"] += c["share"]
+        k["bytes"] += algorithmic_bytes(c["kind"], c["N"], c["K"], c["M"])
+        k["us"] += c["us"]
+        k["calls"].append(c["call"])
+    name = max(kern, key=lambda n: kern[n]["share"])
+    k = kern[name]
+    n = len(k["calls"])
+    achieved = k["bytes"] / k["us"] / 1e3
+    traffic = None
+    if traffic_override is not None:
+        traffic = traffic_override
+    else:
+        t = [measured_traffic(c) for c in k["calls"]]
+        if all(v is not None for v in t):
+            traffic = sum(t) / n
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "kernel": name, "share_of_step": round(k["share"], 4), "launches_per_step": n,
+            "calls": k["calls"], "algorithmic_bytes_per_launch": round(k["bytes"] / n),
+            "us_per_launch": round(k["us"] / n, 3), "peak_source": peaks["source"]}
 
 
 def replica_value(world, step_bytes, ms_max):
@@ -507,6 +560,9 @@ def _oracle_sample(frac_rows):
             q, s, z = oracle.unpack_w4(data, rows, K)
             if kind == "w4a16":
                 oracle.w4a16(x, q, s, z)
+            elif kind == "w4a8r":
+                xq, sx = oracle.act_quant_row(x, K)
+                oracle.w4a8_row(xq, sx, q, s, z)
             else:
                 xq, sx = oracle.act_quant(x, K)
                 oracle.w4a8(xq, sx, q, s, z)
@@ -516,23 +572,35 @@ def _oracle_sample(frac_rows):
     return run, total
 
 
-def cpu_baseline(seconds):
-    import oracle
-    cores = oracle.set_threads(0)
-    run, nbytes = _oracle_sample(0.002)
+def _timed_sample(seconds, start_frac=0.002):
+    """Time the oracle on a sample grown to about `seconds` of host work."""
+    run, nbytes = _oracle_sample(start_frac)
     t0 = time.perf_counter()
     run()
     dt = time.perf_counter() - t0
-    frac = min(1.0, 0.002 * max(1.0, seconds / max(dt, 1e-3)))
-    if frac > 0.002 * 1.5:
+    frac = min(1.0, start_frac * max(1.0, seconds / max(dt, 1e-3)))
+    if frac > start_frac * 1.5:
         run, nbytes = _oracle_sample(frac)
         t0 = time.perf_counter()
         run()
         dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "seconds": round(dt, 2),
-            "sample": "first %.2f%% of the rows (whole 16-row tiles, >= 16) of every call of "
-                      "the step: unpack + dequant + fp64 matmul on the host" % (100 * frac)}
+    return nbytes / dt / 1e9, dt, frac
+
+
+def cpu_baseline(seconds):
+    """The oracle on the host cores: OpenMP over all of them, and one thread."""
+    import oracle
+    cores = oracle.set_threads(0)
+    value, dt, frac = _timed_sample(seconds)
+    oracle.set_threads(1)
+    value1, dt1, frac1 = _timed_sample(seconds / 3, start_frac=0.001)
+    oracle.set_threads(cores)
+    sample = ("first %.2f%% of the rows (whole 16-row tiles, >= 16) of every call of "
+              "the step: unpack + dequant + fp64 matmul on the host")
+    return {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 2), "sample": sample % (100 * frac),
+            "single_thread": {"value": round(value1, 4), "unit": UNIT, "cores": 1,
+                              "seconds": round(dt1, 2), "sample": sample % (100 * frac1)}}
 
 
 def run_reference(args, rank):
@@ -580,7 +648,8 @@ def profile_call(spec, launches):
         fn = lambda: w4q.w8_gemv(x, W, sc)  # noqa: E731
     else:
         packed = w4q.w4_pack_weights(workloads.w4_weight(N, K).to(dev))
-        op = w4q.w4a16_gemm if kind == "w4a16" else w4q.w4a8_gemm
+        op = {"w4a16": w4q.w4a16_gemm, "w4a8": w4q.w4a8_gemm,
+              "w4a8r": w4q.w4a8_gemm_rowscale}[kind]
         ws = torch.empty(max(w4q.workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
         fn = lambda: op(x, packed, N, K, workspace=ws)  # noqa: E731
     for _ in range(2 + launches):

@@ -70,7 +70,7 @@ int check_w4_shape(int64_t M, int64_t N, int64_t K, int group)
 
 int gemm_common(w4q::W4Mode mode, const void *x, const void *packed, void *out, int64_t M,
                 int64_t N, int64_t K, int group, int split, void *workspace,
-                size_t workspace_bytes, int32_t *dots, void *stream)
+                size_t workspace_bytes, int32_t *dots, void *stream, bool act_row = false)
 {
     if (x == nullptr || packed == nullptr || (out == nullptr && dots == nullptr))
         return W4Q_ERR_INVALID_ARG;
@@ -97,7 +97,22 @@ int gemm_common(w4q::W4Mode mode, const void *x, const void *packed, void *out, 
     if (err == nullptr)
         return W4Q_ERR_CUDA;
     cudaError_t e = w4q::launch_w4(plan, mode, x, packed, out, dots, workspace, err,
-                                   static_cast<cudaStream_t>(stream));
+                                   static_cast<cudaStream_t>(stream), act_row);
+    return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
+}
+
+int quantize_act_common(const void *x_bf16, int64_t M, int64_t K, int8_t *xq, float *sx,
+                        bool row, void *stream)
+{
+    if (x_bf16 == nullptr || xq == nullptr || sx == nullptr)
+        return W4Q_ERR_INVALID_ARG;
+    int st = check_w4_shape(M, 1, K, 32);
+    if (st != W4Q_OK)
+        return st;
+    if (!aligned16(x_bf16) || !aligned16(xq) || !aligned16(sx))
+        return W4Q_ERR_MISALIGNED;
+    cudaError_t e = w4q::launch_act_quant_i8(x_bf16, (int)M, (int)K, xq, sx, row,
+                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
 }
 
@@ -218,8 +233,11 @@ int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8)
     w4q::W4Plan plan;
     if (!w4q::w4_plan((int)M, (int)N, (int)K, -1, sm_count(dev), mode, &plan))
         return -1;
-    // the activation preparation (and counter reset), the main kernel, and
-    // for the tensor-core kernel with split row groups the partial-sum launch
+    // the cluster kernel alone; else the activation preparation (and counter
+    // reset), the main kernel, and for the tensor-core kernel with split row
+    // groups the partial-sum launch
+    if (plan.cluster > 0)
+        return 1;
     return (plan.umma && plan.fixup) ? 3 : 2;
 }
 
@@ -260,16 +278,13 @@ int w4a8_gemm_split(const void *x_bf16, const void *packed, void *out_bf16, int6
 int w4a8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq, float *sx,
                       void *stream)
 {
-    if (x_bf16 == nullptr || xq == nullptr || sx == nullptr)
-        return W4Q_ERR_INVALID_ARG;
-    int st = check_w4_shape(M, 1, K, 32);
-    if (st != W4Q_OK)
-        return st;
-    if (!aligned16(x_bf16) || !aligned16(xq) || !aligned16(sx))
-        return W4Q_ERR_MISALIGNED;
-    cudaError_t e = w4q::launch_act_quant_i8(x_bf16, (int)M, (int)K, xq, sx,
-                                             static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
+    return quantize_act_common(x_bf16, M, K, xq, sx, false, stream);
+}
+
+int w4a8_quantize_act_rowscale(const void *x_bf16, int64_t M, int64_t K, int8_t *xq, float *sx,
+                               void *stream)
+{
+    return quantize_act_common(x_bf16, M, K, xq, sx, true, stream);
 }
 
 int w4a8_group_dots(const void *x_bf16, const void *packed, int64_t M, int64_t N, int64_t K,
@@ -277,8 +292,36 @@ int w4a8_group_dots(const void *x_bf16, const void *packed, int64_t M, int64_t N
 {
     if (D == nullptr)
         return W4Q_ERR_INVALID_ARG;
-    return gemm_common(w4q::W4Mode::A8_DOTS, x_bf16, packed, nullptr, M, N, K, group, 1,
+    return gemm_common(w4q::W4Mode::A8_DOTS, x_bf16, packed, nullptr, M, N, K, group, -1,
                        workspace, workspace_bytes, D, stream);
+}
+
+int w4a8_group_dots_rowscale(const void *x_bf16, const void *packed, int64_t M, int64_t N,
+                             int64_t K, int group, int32_t *D, void *workspace,
+                             size_t workspace_bytes, void *stream)
+{
+    if (D == nullptr)
+        return W4Q_ERR_INVALID_ARG;
+    return gemm_common(w4q::W4Mode::A8_DOTS, x_bf16, packed, nullptr, M, N, K, group, -1,
+                       workspace, workspace_bytes, D, stream, true);
+}
+
+int w4a8_gemm_rowscale(const void *x_bf16, const void *packed, void *out_bf16, int64_t M,
+                       int64_t N, int64_t K, int group, void *workspace, size_t workspace_bytes,
+                       void *stream)
+{
+    return gemm_common(w4q::W4Mode::A8, x_bf16, packed, out_bf16, M, N, K, group, -1, workspace,
+                       workspace_bytes, nullptr, stream, true);
+}
+
+int w4a8_gemm_rowscale_split(const void *x_bf16, const void *packed, void *out_bf16, int64_t M,
+                             int64_t N, int64_t K, int group, int split_k, void *workspace,
+                             size_t workspace_bytes, void *stream)
+{
+    if (split_k < 0)
+        return W4Q_ERR_INVALID_ARG;
+    return gemm_common(w4q::W4Mode::A8, x_bf16, packed, out_bf16, M, N, K, group, split_k,
+                       workspace, workspace_bytes, nullptr, stream, true);
 }
 
 int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16, void *out_bf16,

@@ -1,0 +1,535 @@
+// gemv_w4_cluster.cu -- decode-sized W4A16 / W4A8 linear layer for 1 <= M <= 8
+// on sm_103a, one thread-block cluster per 128-row group:
+//
+//   out[M,N] = x[M,K] . dequant(Wq)[N,K]^T,   dequant(q) = (q - z) * s
+//
+// ("test_int4_quantized_gemm.py": the dequant + F.linear reference and the
+// W4A8 bucket kernels; a GB300 design of this library, not their code.)
+//
+// One launch per call, no workspace:
+//  * The grid is (C, G): cluster g (C CTAs along x) owns the 128-row group g
+//    of the packed weight, and its CTA of rank r streams the contiguous
+//    super-blocks [r*KB/C, (r+1)*KB/C) of K (KB = K/256).  C is the call's
+//    K split (1..8).
+//  * The weight stream of each CTA starts before griddepcontrol.wait: the
+//    first stages are in flight while the kernel before it on the stream
+//    finishes (the weights are not written by that kernel).
+//  * After the wait, all nine warps prepare the CTA's slice of the
+//    activations in shared memory, once for all its stages:
+//      W4A16: per row and super-block a power-of-two prescale sigma,
+//             x' = x * 2^sigma (2^(sigma-4) on the upper eight columns of
+//             every 16-column step), X'[g] = 2^(sigma-133) * sum_{k in g} x,
+//             c = 2^(133 - sigma);
+//      W4A8:  symmetric int8 xq = clamp(rint(x / sx), -127, 127) in IEEE
+//             fp32, with sx = fp32(max|x| / 127) over a group of 32 or over
+//             the whole row; x' = xq * 2^121 (2^117 upper), X' = 2^-12 *
+//             sum xq, and sx * 2^12 per group.  The row scale needs the max
+//             over all of K: each CTA reduces its slice, the cluster
+//             exchanges the C partial maxima through distributed shared
+//             memory, and every CTA takes the max of them.
+//  * Eight consumer warps each own one 16-row tile and run the same stage
+//    arithmetic as the stream-K kernel (w4_stage.cuh): bf16 m16n8k16 MMAs on
+//    the masked nibbles, exact per-group dots, the fp32 scale / zero update.
+//  * Split-K reduction: each CTA leaves its 128 x M fp32 sums in its shared
+//    memory; after a cluster barrier, CTA r sums the C CTAs' values of rows
+//    [r*128/C, (r+1)*128/C) over distributed shared memory in rank order
+//    (fixed order: the result does not depend on timing) and writes them
+//    as bf16.  A second cluster barrier keeps every CTA's shared memory
+//    alive until its peers have read it.
+//  * Every ring wait is bounded (one second of %globaltimer): on expiry the
+//    kernel sets a bit in the error word, still passes the cluster barriers
+//    (every thread reaches them on every path), drains its copies and
+//    returns.
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "w4_stage.cuh"
+
+#ifdef W4Q_SPIN_WAITS
+#define W4Q_RING_WAIT mbar_wait_bounded
+#else
+#define W4Q_RING_WAIT mbar_wait_sleep
+#endif
+
+namespace w4q {
+
+namespace {
+
+constexpr int MAX_CLUSTER = 8;   // portable cluster size
+constexpr int CTA_SMEM_MAX = 113 * 1024;  // two CTAs per SM
+
+struct CParams {
+    const uint8_t *packed;
+    const __nv_bfloat16 *x;  // bf16 [M][K], as given
+    __nv_bfloat16 *out;      // bf16 [M][N]
+    int32_t *dots;           // W4A8 group-dot export: int32 [M][N][K/32]
+    unsigned *err;
+    int M, N, K, KB, T, G, C, smax, R;  // R: weight ring stages (2..4)
+};
+
+// ------------------------------------------------------------ cluster PTX
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Barrier over every thread of every CTA of the cluster; shared-memory
+// writes before it are visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of this CTA's shared-memory address `addr` in
+// the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank)
+{
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ----------------------------------------------------------- smem layout
+
+struct CLayout {
+    int ring, xr, xs, xg, red, rowmax, zero, bars, total;
+};
+
+// [ring: R x 19456][x': smax x MP x 528][X': smax x MP x 32][factors:
+// smax x MP x 32][partial sums: 128 x MP f32][row maxima: 8 u32][16 zero
+// bytes][barriers: 2R x 8]
+__host__ __device__ inline CLayout c_layout(int mp, int smax, int R)
+{
+    CLayout L;
+    int o = 0;
+    L.ring = o;
+    o += R * WARPS * TILE_BYTES;
+    L.xr = o;
+    o += smax * mp * XROW;
+    L.xs = o;
+    o += smax * mp * SROW;
+    L.xg = o;
+    o += smax * mp * SROW;
+    L.red = o;
+    o += GROUP_ROWS * mp * 4;
+    L.rowmax = o;
+    o += 32;
+    L.zero = o;
+    o += 16;
+    L.bars = o;
+    o += 2 * R * 8;
+    L.total = (o + 127) / 128 * 128;
+    return L;
+}
+
+// W4A8: one super-block's int8 activations from the raw bf16 of MP rows
+// (lane l holds columns 8l .. 8l + 7), with the scale of the lane's group of
+// 32 (its 4 lanes) or, ROW, of the whole row (arow = the row's max |x|):
+// x' = xq * 2^121 (2^117 on the odd lanes, the upper half of a 16-column
+// step), X'[g] = 2^-12 * sum xq, and the group scale sx * 2^12.
+template <int MP, bool ROW>
+__device__ __forceinline__ void prep_stage_a8(const uint4 (&raw)[MP], int M, int lane,
+                                              const float (&arow)[MP], uint8_t *xdst,
+                                              uint8_t *sdst, uint8_t *gdst)
+{
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+        const uint32_t w[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = bf16lo_to_f32(w[j]);
+            v[2 * j + 1] = bf16hi_to_f32(w[j]);
+        }
+        float a = 0.f;
+        if (ROW) {
+            a = arow[m];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                a = fmaxf(a, fabsf(v[j]));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        }
+        const float sx = __fdiv_rn(a, 127.0f);
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sx)), -127.f), 127.f);
+            part += v[j];
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        // |xq| <= 127 has at most 7 significant bits: xq * 2^sh is exact in bf16
+        const float f = __uint_as_float((uint32_t)(((lane & 1) ? 117 : 121) + 127) << 23);
+        uint32_t ow[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * j] * f, v[2 * j + 1] * f);
+            ow[j] = *reinterpret_cast<const uint32_t *>(&h2);
+        }
+        if (m < M) {
+            *reinterpret_cast<uint4 *>(xdst + m * XROW + 16 * lane) =
+                make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            if ((lane & 3) == 0) {
+                *reinterpret_cast<float *>(sdst + m * SROW + 4 * (lane >> 2)) = part * 0x1p-12f;
+                *reinterpret_cast<float *>(gdst + m * SROW + 4 * (lane >> 2)) = sx * 4096.0f;
+            }
+        }
+    }
+}
+
+template <W4Mode MODE, bool ROW, int MP>
+__global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
+{
+    constexpr bool DOTS = MODE == W4Mode::A8_DOTS;
+    constexpr bool A16 = MODE == W4Mode::A16;
+    constexpr int SB = WARPS * TILE_BYTES;  // one stage: the 8 tiles of a super-block
+    const int R = p.R;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    const CLayout L = c_layout(MP, p.smax, R);
+    uint8_t *xr = smem + L.xr, *xs = smem + L.xs, *xg = smem + L.xg;
+    float *red = reinterpret_cast<float *>(smem + L.red);
+    uint32_t *rowmax = reinterpret_cast<uint32_t *>(smem + L.rowmax);
+    const uint32_t full0 = smem_addr(smem + L.bars), empty0 = full0 + 8 * R;
+    const uint32_t zrow = smem_addr(smem + L.zero);
+
+    // hardware warp 0 produces (the schedulers favour low warp ids); 1..8
+    // are the consumers of row tiles 0..7
+    const int hw_warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = hw_warp == 0 ? WARPS : hw_warp - 1;
+    const uint32_t rank = cluster_rank();
+    const int g = blockIdx.y;
+    const int b0 = (int)((long long)rank * p.KB / p.C);
+    const int S = (int)((long long)(rank + 1) * p.KB / p.C) - b0;  // stages of this CTA
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, WARPS);
+        }
+        fence_barrier_init();
+    }
+    // zero: the 16-byte zero row, the row maxima, and the activation rows
+    // m >= M of every stage (read by the MMAs, never stored)
+    if (threadIdx.x < 8)
+        rowmax[threadIdx.x] = 0u;
+    if (threadIdx.x == 8)
+        *reinterpret_cast<uint4 *>(smem + L.zero) = make_uint4(0u, 0u, 0u, 0u);
+    {
+        const int pad = MP - p.M;
+        const int xper = pad * (XROW / 16), sper = pad * (SROW / 16);
+        const int per = xper + 2 * sper;
+        for (int i = threadIdx.x; i < S * per; i += THREADS) {
+            const int s = i / per, rem = i % per;
+            uint8_t *dst;
+            if (rem < xper)
+                dst = xr + (s * MP + p.M + rem / (XROW / 16)) * XROW + (rem % (XROW / 16)) * 16;
+            else if (rem < xper + sper)
+                dst = xs + (s * MP + p.M + (rem - xper) / 2) * SROW + ((rem - xper) % 2) * 16;
+            else
+                dst = xg + (s * MP + p.M + (rem - xper - sper) / 2) * SROW +
+                      ((rem - xper - sper) % 2) * 16;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __syncthreads();
+    pdl_launch_dependents();  // the next kernel on the stream may launch and prefetch
+
+    // -------------------------------------------- weight prefetch (no wait)
+    const uint8_t *wsrc = p.packed + ((size_t)g * p.KB + b0) * SB;
+    int issued = 0;
+    const int pro = S < R ? S : R;
+    if (warp == WARPS && lane == 0) {
+        const uint64_t pol = policy_evict_first();
+        for (int i = 0; i < pro; ++i) {
+            mbar_arrive_expect_tx(full0 + 8 * i, (uint32_t)SB);
+            bulk_g2s(smem_addr(smem + L.ring + i * SB), wsrc + (size_t)i * SB, SB, full0 + 8 * i,
+                     pol);
+        }
+        issued = pro;
+    }
+
+    // ------------------------------------- the slice's activation operand
+    pdl_wait();  // x may come from the kernel launched before this one
+    if constexpr (A16) {
+        for (int s = hw_warp; s < S; s += WARPS + 1) {
+            uint4 raw[MP];
+            load_stage_a16<MP>(p.x, p.M, p.K, b0 + s, lane, raw);
+            prep_stage_a16<MP>(raw, p.M, lane, xr + s * MP * XROW, xs + s * MP * SROW,
+                               xg + s * MP * SROW);
+        }
+    } else {
+        float arow[MP];
+#pragma unroll
+        for (int m = 0; m < MP; ++m)
+            arow[m] = 0.f;
+        if constexpr (ROW) {
+            // pass 1: the raw slice into the x' rows, and this CTA's max |x| per row
+            for (int s = hw_warp; s < S; s += WARPS + 1) {
+                uint4 raw[MP];
+                load_stage_a16<MP>(p.x, p.M, p.K, b0 + s, lane, raw);
+#pragma unroll
+                for (int m = 0; m < MP; ++m) {
+                    uint32_t h = __vmaxu2(__vmaxu2(raw[m].x & 0x7FFF7FFFu, raw[m].y & 0x7FFF7FFFu),
+                                          __vmaxu2(raw[m].z & 0x7FFF7FFFu, raw[m].w & 0x7FFF7FFFu));
+                    h = max(h & 0xFFFFu, h >> 16);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        h = max(h, __shfl_xor_sync(0xffffffffu, h, o));
+                    if (m < p.M) {
+                        *reinterpret_cast<uint4 *>(xr + (s * MP + m) * XROW + 16 * lane) = raw[m];
+                        if (lane == 0)
+                            atomicMax(&rowmax[m], h);
+                    }
+                }
+            }
+            cluster_sync();  // every CTA's slice maxima are written
+            // the row's max over the C slices (magnitudes order as bf16 bits)
+            const uint32_t base = smem_addr(rowmax);
+#pragma unroll
+            for (int m = 0; m < MP; ++m) {
+                uint32_t h = 0u;
+                for (int c = 0; c < p.C; ++c)
+                    h = max(h, ld_peer_u32(peer_addr(base + 4 * m, (uint32_t)c)));
+                arow[m] = __uint_as_float(h << 16);
+            }
+        }
+        for (int s = hw_warp; s < S; s += WARPS + 1) {
+            uint4 raw[MP];
+            if constexpr (ROW) {
+#pragma unroll
+                for (int m = 0; m < MP; ++m)
+                    raw[m] = m < p.M ? *reinterpret_cast<const uint4 *>(xr + (s * MP + m) * XROW +
+                                                                        16 * lane)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+                __syncwarp();  // every lane has read its raw chunk before any is overwritten
+            } else {
+                load_stage_a16<MP>(p.x, p.M, p.K, b0 + s, lane, raw);
+            }
+            prep_stage_a8<MP, ROW>(raw, p.M, lane, arow, xr + s * MP * XROW, xs + s * MP * SROW,
+                                   xg + s * MP * SROW);
+        }
+    }
+    __syncthreads();  // the slice's activation operand is complete
+
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    const int tile = g * WARPS + warp;
+    if (warp == WARPS) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            for (int i = pro; i < S; ++i) {
+                const int slot = i % R;
+                if (!W4Q_RING_WAIT(empty0 + 8 * slot, (uint32_t)(i / R - 1) & 1)) {
+                    report_error(p.err, ERR_EMPTY_WAIT);
+                    break;
+                }
+                mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)SB);
+                bulk_g2s(smem_addr(smem + L.ring + slot * SB), wsrc + (size_t)i * SB, SB,
+                         full0 + 8 * slot, pol);
+                issued = i + 1;
+            }
+        }
+    } else {
+        // ----------------------------------------------------- consumers
+        for (int i = 0; i < S; ++i) {
+            const int slot = i % R;
+            if (!W4Q_RING_WAIT(full0 + 8 * slot, (uint32_t)(i / R) & 1)) {
+                report_error(p.err, ERR_FULL_WAIT);
+                break;
+            }
+            if (tile < p.T) {
+                const uint32_t wbase = smem_addr(smem + L.ring + slot * SB + warp * TILE_BYTES);
+                const uint32_t xb = smem_addr(xr + i * MP * XROW);
+                const uint32_t sb = smem_addr(xs + i * MP * SROW);
+                const uint32_t gb = smem_addr(xg + i * MP * SROW);
+                if constexpr (MP < 8)
+                    compute_stage_packed<MP, DOTS, !A16, A16>(wbase, xb, sb, gb, zrow, lane, acc, p,
+                                                              tile, b0 + i);
+                else
+                    compute_stage<1, DOTS, !A16, A16>(wbase, xb, sb, gb, lane, acc, p, tile,
+                                                      b0 + i);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8 * slot);
+        }
+        if (!DOTS) {
+            // add the accumulator slots (lanes of one row hold other groups of
+            // the same outputs), then park this warp's 16 x MP sums
+            const int r = lane >> 2, c2 = 2 * (lane & 3);
+            if constexpr (MP < 8) {
+                if (MP == 1) {
+                    acc[0][0] += acc[0][1];
+                    acc[0][2] += acc[0][3];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (MP <= 2)
+                        acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], 1);
+                    acc[0][e] += __shfl_xor_sync(0xffffffffu, acc[0][e], 2);
+                }
+            }
+            if (c2 < MP) {  // slot 0 of the columns: (row, m) = (r or r + 8, c2 + (e & 1))
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = c2 + (e & 1);
+                    if (MP == 1 && (e & 1))
+                        continue;
+                    if (m < MP)
+                        red[(warp * 16 + r + 8 * (e >> 1)) * MP + m] = acc[0][e];
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------- split-K over the cluster
+    cluster_sync();  // every CTA's partial sums are in its shared memory
+    if (!DOTS) {
+        const int C = p.C;
+        const int r0 = (int)(rank * GROUP_ROWS / C), r1 = (int)((rank + 1) * GROUP_ROWS / C);
+        const int nr = r1 - r0;
+        const uint32_t rbase = smem_addr(red);
+        for (int t = threadIdx.x; t < nr * p.M; t += THREADS) {
+            const int row = r0 + t % nr, m = t / nr;
+            const uint32_t a = rbase + 4 * (row * MP + m);
+            float v = ld_peer_f32(peer_addr(a, 0u));
+            for (int c = 1; c < C; ++c)
+                v += ld_peer_f32(peer_addr(a, (uint32_t)c));
+            const int n = g * GROUP_ROWS + row;
+            if (n < p.N)
+                p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
+        }
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+
+    // Drain: every issued stage's copy must have landed before the shared
+    // memory goes away (only the error path can leave one pending).
+    if (warp == WARPS && lane == 0) {
+        for (int s = 0; s < R && s < issued; ++s) {
+            const int last_use = (issued - 1 - s) / R;
+            if (!W4Q_RING_WAIT(full0 + 8 * s, (uint32_t)last_use & 1)) {
+                report_error(p.err, ERR_DRAIN_WAIT);
+                break;
+            }
+        }
+    }
+}
+
+template <W4Mode MODE, bool ROW, int MP>
+cudaError_t launch_t(const CParams &p, int smem, cudaStream_t stream)
+{
+    auto fn = w4_cluster_kernel<MODE, ROW, MP>;
+    // the dynamic shared-memory opt-in, once per device (a bit per device)
+    static std::atomic<unsigned long long> opted_in{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit == 0 || !(opted_in.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, CTA_SMEM_MAX);
+        if (e != cudaSuccess)
+            return e;
+        opted_in.fetch_or(bit, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.C, (unsigned)p.G);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <W4Mode MODE, bool ROW>
+cudaError_t dispatch_mp(const CParams &p, int mp, int smem, cudaStream_t stream)
+{
+    switch (mp) {
+    case 1: return launch_t<MODE, ROW, 1>(p, smem, stream);
+    case 2: return launch_t<MODE, ROW, 2>(p, smem, stream);
+    case 4: return launch_t<MODE, ROW, 4>(p, smem, stream);
+    default: return launch_t<MODE, ROW, 8>(p, smem, stream);
+    }
+}
+
+int mp_of(int M) { return M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8)); }
+
+}  // namespace
+
+// The weight-ring depth for these sizes (4 stages, fewer where the slice's
+// activation operand needs the room), or 0 when even 2 do not fit in the
+// shared memory of one of two CTAs per SM.
+int w4_cluster_ring(int M, int KB, int C)
+{
+    if (C < 1 || C > MAX_CLUSTER || C > KB || M < 1 || M > 8)
+        return 0;
+    const int smax = (KB + C - 1) / C;
+    for (int R = 4; R >= 2; --R)
+        if (c_layout(mp_of(M), smax, R).total <= CTA_SMEM_MAX)
+            return R;
+    return 0;
+}
+
+cudaError_t launch_w4_cluster(const W4Plan &plan, W4Mode mode, bool act_row, const void *x,
+                              const void *packed, void *out, int32_t *dots, unsigned *err,
+                              cudaStream_t stream)
+{
+    CParams p;
+    p.packed = static_cast<const uint8_t *>(packed);
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.dots = dots;
+    p.err = err;
+    p.M = plan.M;
+    p.N = plan.N;
+    p.K = plan.K;
+    p.KB = plan.KB;
+    p.T = plan.T;
+    p.G = plan.G;
+    p.C = plan.cluster;
+    p.smax = (plan.KB + plan.cluster - 1) / plan.cluster;
+    p.R = w4_cluster_ring(plan.M, plan.KB, plan.cluster);
+    if (p.R == 0)
+        return cudaErrorInvalidValue;
+    const int mp = mp_of(plan.M);
+    const int smem = c_layout(mp, p.smax, p.R).total;
+    if (mode == W4Mode::A16)
+        return dispatch_mp<W4Mode::A16, false>(p, mp, smem, stream);
+    if (mode == W4Mode::A8)
+        return act_row ? dispatch_mp<W4Mode::A8, true>(p, mp, smem, stream)
+                       : dispatch_mp<W4Mode::A8, false>(p, mp, smem, stream);
+    return act_row ? dispatch_mp<W4Mode::A8_DOTS, true>(p, mp, smem, stream)
+                   : dispatch_mp<W4Mode::A8_DOTS, false>(p, mp, smem, stream);
+}
+
+}  // namespace w4q

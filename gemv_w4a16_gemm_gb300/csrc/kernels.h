@@ -31,6 +31,7 @@ struct W4Plan {
     bool umma;      // tcgen05 kernel (W4A16, M >= 9): units are pairs of tile groups
     int NP;         // umma: M rounded up to 16 (the MMA's N)
     int G2;         // umma: ceil(G / 2) pairs of tile groups
+    int cluster;    // > 0: the cluster kernel (M <= 8), this many CTAs split each group's K
 };
 
 enum class W4Mode { A16, A8, A8_DOTS };
@@ -42,9 +43,18 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
 // Workspace bytes for a plan (partials + the W4A8 activation buffers).
 size_t w4_workspace_for(const W4Plan &plan, W4Mode mode);
 
+// act_row: W4A8 with one activation scale per row (else per group of 32).
 cudaError_t launch_w4(const W4Plan &plan, W4Mode mode, const void *x, const void *packed,
                       void *out, int32_t *dots, void *workspace, unsigned *err,
-                      cudaStream_t stream);
+                      cudaStream_t stream, bool act_row = false);
+
+// --- W4A16 / W4A8 at M <= 8, one thread-block cluster per 128-row group
+// (gemv_w4_cluster.cu).  w4_cluster_ring: the ring depth for a K split of C
+// CTAs, 0 when the call does not fit the kernel's shared memory.
+int w4_cluster_ring(int M, int KB, int C);
+cudaError_t launch_w4_cluster(const W4Plan &plan, W4Mode mode, bool act_row, const void *x,
+                              const void *packed, void *out, int32_t *dots, unsigned *err,
+                              cudaStream_t stream);
 
 // --- W4A16 on the tcgen05 tensor core, 9 <= M <= 64 (gemv_w4_umma.cu)
 size_t w4_umma_workspace(const W4Plan &plan);
@@ -52,7 +62,7 @@ size_t w4_umma_partial_bytes(int P, int M);
 cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed, void *out,
                            void *workspace, unsigned *err, cudaStream_t stream);
 
-cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *sx,
+cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *sx, bool row,
                                 cudaStream_t stream);
 
 // --- per-device state kept by api.cu

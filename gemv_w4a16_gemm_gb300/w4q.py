@@ -45,6 +45,10 @@ SIGNATURES = {
     "w4a8_gemm_split": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _SZ, _P]),
     "w4a8_quantize_act": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "w4a8_group_dots": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, _P, _SZ, _P]),
+    "w4a8_gemm_rowscale": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _P, _SZ, _P]),
+    "w4a8_gemm_rowscale_split": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _INT, _P, _SZ, _P]),
+    "w4a8_quantize_act_rowscale": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "w4a8_group_dots_rowscale": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, _P, _SZ, _P]),
     "w8_gemv": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4q_device_error": (_INT, [_U32P]),
 }
@@ -194,27 +198,55 @@ def w4a16_gemm_noalloc(x, packed, N, K, group=GROUP, out=None, stream=None):
 
 
 def w4a8_gemm(x, packed, N, K, group=GROUP, split_k=None, out=None, workspace=None, stream=None):
-    """out[M,N] = x . dequant(packed)^T with per-row int8 activations (W4A8)."""
+    """out[M,N] = x . dequant(packed)^T, W4A8 with one int8 activation scale
+    per (row, group of 32)."""
     return _gemm("w4a8_gemm", x, packed, N, K, group, split_k, out, workspace, stream)
 
 
-def w4a8_quantize_act(x: torch.Tensor, stream=None):
+def w4a8_gemm_rowscale(x, packed, N, K, group=GROUP, split_k=None, out=None, workspace=None,
+                       stream=None):
+    """out[M,N] = x . dequant(packed)^T, W4A8 with one int8 activation scale
+    per row (absmax / 127)."""
+    return _gemm("w4a8_gemm_rowscale", x, packed, N, K, group, split_k, out, workspace, stream)
+
+
+def _quantize_act(name, x, row, stream):
     M, K = x.shape
     xq = torch.empty(M, K, dtype=torch.int8, device=x.device)
-    sx = torch.empty(M, K // GROUP, dtype=torch.float32, device=x.device)
-    _check("w4a8_quantize_act", lib().w4a8_quantize_act(
+    sx = torch.empty((M,) if row else (M, K // GROUP), dtype=torch.float32, device=x.device)
+    _check(name, getattr(lib(), name)(
         _cuda(x, torch.bfloat16, "x"), M, K, xq.data_ptr(), sx.data_ptr(), _stream(stream)))
     return xq, sx
 
 
-def w4a8_group_dots(x, packed, N, K, group=GROUP, workspace=None, stream=None):
+def w4a8_quantize_act(x: torch.Tensor, stream=None):
+    """(xq int8 [M,K], sx fp32 [M, K/32]): the per-group W4A8 quantizer."""
+    return _quantize_act("w4a8_quantize_act", x, False, stream)
+
+
+def w4a8_quantize_act_rowscale(x: torch.Tensor, stream=None):
+    """(xq int8 [M,K], sx fp32 [M]): the per-row W4A8 quantizer."""
+    return _quantize_act("w4a8_quantize_act_rowscale", x, True, stream)
+
+
+def _group_dots(name, x, packed, N, K, group, workspace, stream):
     M = x.shape[0]
     D = torch.empty(M, N, K // group, dtype=torch.int32, device=x.device)
     ws, wsb = _workspace(M, N, K, group, None, workspace, x.device)
-    _check("w4a8_group_dots", lib().w4a8_group_dots(
+    _check(name, getattr(lib(), name)(
         _cuda(x, torch.bfloat16, "x"), _cuda(packed, torch.uint8, "packed"), M, N, K, group,
         D.data_ptr(), ws.data_ptr(), wsb, _stream(stream)))
     return D
+
+
+def w4a8_group_dots(x, packed, N, K, group=GROUP, workspace=None, stream=None):
+    """Exact int32 W4A8 group dots [M, N, K/32] (per-group activation scales)."""
+    return _group_dots("w4a8_group_dots", x, packed, N, K, group, workspace, stream)
+
+
+def w4a8_group_dots_rowscale(x, packed, N, K, group=GROUP, workspace=None, stream=None):
+    """Exact int32 W4A8 group dots [M, N, K/32] (per-row activation scales)."""
+    return _group_dots("w4a8_group_dots_rowscale", x, packed, N, K, group, workspace, stream)
 
 
 def w8_gemv(x, W, scales, out=None, stream=None):

@@ -10,9 +10,11 @@
  *          QuantConfig(bits=4, group_size=32, symmetric=False,
  *          method="min_max"); the dequant + F.linear reference.)
  *   W4A8   the same weights, activations quantized to symmetric int8
- *          inside the call with one scale per (row, group of 32); each
- *          group's dot product is an exact integer, scaled in fp32.  ("test_int4_quantized_gemm.py": the
- *          W4A8 bucket kernels and Int4QuantizedGemmPrecisionTest.)
+ *          inside the call, with one scale per whole row (w4a8_gemm_rowscale,
+ *          scale = max|x| / 127 over the row) or one per (row, group of 32)
+ *          (w4a8_gemm); each group's dot product is an exact integer, scaled
+ *          in fp32.  ("test_int4_quantized_gemm.py": the W4A8 bucket kernels
+ *          and Int4QuantizedGemmPrecisionTest.)
  *   W8     int8 weights with one bf16 scale per output row.
  *          ("gpt-fast issue #114": WeightOnlyInt8Linear.forward,
  *          F.linear(x, W.to(bf16)) * scales, and its fused reduction.)
@@ -213,10 +215,35 @@ int w4a8_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
                     int64_t M, int64_t N, int64_t K, int group, int split_k,
                     void *workspace, size_t workspace_bytes, void *stream);
 
+/* out = x . dequant(packed)^T, W4A8 with one activation scale per row:
+ * per row m, sx[m] = fp32(max_k |x[m,k]| / 127), xq = clamp(rint(x /
+ * sx[m]), -127, 127) in IEEE fp32 (xq = 0 for an all-zero row); per group
+ * D = sum_k (q - z) * xq, an exact integer; acc = sum_g (sx[m] * s_g) * D_g
+ * in fp32; out = bf16_RN(acc).  Symmetric int8 activations with the scale
+ * absmax / 127 per row, as the W4A8 bucket kernels of
+ * "test_int4_quantized_gemm.py" are exercised on gaussian activations
+ * (Int4QuantizedGemmPrecisionTest: mean |a8 - a16| / mean |a16| < 0.02).
+ * A few large outlier channels flatten the rest of their row under this
+ * rule; w4a8_gemm (one scale per group of 32) is the variant for them.
+ * Arguments, limits and workspace as w4a8_gemm. */
+int w4a8_gemm_rowscale(const void *x_bf16, const void *packed, void *out_bf16,
+                       int64_t M, int64_t N, int64_t K, int group,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+int w4a8_gemm_rowscale_split(const void *x_bf16, const void *packed,
+                             void *out_bf16, int64_t M, int64_t N, int64_t K,
+                             int group, int split_k, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
 /* The W4A8 activation quantizer alone (the rule w4a8_gemm applies).
  *   xq  device, int8 [M,K] (written);  sx  device, f32 [M][K/32] (written). */
 int w4a8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq,
                       float *sx, void *stream);
+
+/* The per-row W4A8 activation quantizer alone (the rule w4a8_gemm_rowscale
+ * applies).  xq  device, int8 [M,K] (written);  sx  device, f32 [M]. */
+int w4a8_quantize_act_rowscale(const void *x_bf16, int64_t M, int64_t K,
+                               int8_t *xq, float *sx, void *stream);
 
 /* The exact W4A8 group dot products, for bit-exact checks (1 <= M <= 8).
  *   D          device, int32 [M][N][K/32] (written)
@@ -226,6 +253,13 @@ int w4a8_quantize_act(const void *x_bf16, int64_t M, int64_t K, int8_t *xq,
 int w4a8_group_dots(const void *x_bf16, const void *packed, int64_t M,
                     int64_t N, int64_t K, int group, int32_t *D,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* As w4a8_group_dots, with the per-row activation quantizer of
+ * w4a8_gemm_rowscale. */
+int w4a8_group_dots_rowscale(const void *x_bf16, const void *packed, int64_t M,
+                             int64_t N, int64_t K, int group, int32_t *D,
+                             void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /* ---------------------------------------------------------------- W8 --- */
 

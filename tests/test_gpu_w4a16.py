@@ -44,19 +44,16 @@ def test_gemv_model_shapes_full(cuda, N, K):
 
 @pytest.mark.parametrize("N,K", workloads.TC_SHAPES)
 def test_skinny_gemm_shapes(cuda, N, K):
-    # M = 16 / 64 on the full shapes; the 39936 x 6656 M = 64 oracle is the
-    # slowest case (about 17 G multiply-adds), so outputs are compared on a
-    # window of rows there and in full elsewhere.
+    # M = 16 / 64 on the full shapes, every output against the oracle (the
+    # 39936 x 6656 M = 64 case is about 17 G multiply-adds on the host).  The
+    # output starts as NaN, so a row the kernels never write fails.
     W, q, s, z = quantized(N, K)
     packed = w4q.w4_pack_weights(W.to(cuda))
     for M in workloads.TC_MS:
         x = workloads.activation(M, K, seed=workloads.x_seed(N, K, M))
-        out = w4q.w4a16_gemm(x.to(cuda), packed, N, K)
-        if N * K * M > 6e9:
-            for a, b in ((0, 256), (N // 2, N // 2 + 128), (N - 200, N)):
-                assert_close(out[:, a:b], oracle.w4a16(x, q, s, z, a, b), "M=%d rows %d:%d" % (M, a, b))
-        else:
-            assert_close(out, oracle.w4a16(x, q, s, z), "N=%d K=%d M=%d" % (N, K, M))
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=cuda)
+        w4q.w4a16_gemm(x.to(cuda), packed, N, K, out=out)
+        assert_close(out, oracle.w4a16(x, q, s, z), "N=%d K=%d M=%d" % (N, K, M))
 
 
 def test_every_legal_split_matches(cuda):
