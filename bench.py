@@ -253,7 +253,8 @@ class Suite:
     def launches_per_step(self):
         n = 0
         for kind, N, K, M in self.calls:
-            n += 1 if kind == "w8" else self.w4q.kernel_launches(M, N, K, kind != "w4a16")
+            n += 1 if kind == "w8" else self.w4q.kernel_launches(
+                M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
         return n
 
     def step_copy_index(self, i):

@@ -88,7 +88,7 @@ int gemm_common(w4q::W4Mode mode, const void *x, const void *packed, void *out, 
     if (dev < 0)
         return W4Q_ERR_CUDA;
     w4q::W4Plan plan;
-    if (!w4q::w4_plan((int)M, (int)N, (int)K, split, sm_count(dev), mode, &plan))
+    if (!w4q::w4_plan((int)M, (int)N, (int)K, split, sm_count(dev), mode, &plan, act_row))
         return W4Q_ERR_UNSUPPORTED;
     const size_t need = w4q::w4_workspace_for(plan, mode);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
@@ -124,10 +124,12 @@ size_t workspace_common(int64_t M, int64_t N, int64_t K, int group, int split)
     if (dev < 0)
         return 0;
     size_t best = 0;
-    const w4q::W4Mode modes[2] = {w4q::W4Mode::A16, w4q::W4Mode::A8};
-    for (w4q::W4Mode mode : modes) {
+    // W4A16, W4A8 with a scale per group, W4A8 with a scale per row
+    const w4q::W4Mode modes[3] = {w4q::W4Mode::A16, w4q::W4Mode::A8, w4q::W4Mode::A8};
+    for (int v = 0; v < 3; ++v) {
+        const w4q::W4Mode mode = modes[v];
         w4q::W4Plan plan;
-        if (w4q::w4_plan((int)M, (int)N, (int)K, split, sm_count(dev), mode, &plan)) {
+        if (w4q::w4_plan((int)M, (int)N, (int)K, split, sm_count(dev), mode, &plan, v == 2)) {
             const size_t b = w4q::w4_workspace_for(plan, mode);
             if (b > best)
                 best = b;
@@ -229,9 +231,11 @@ int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8)
     const int dev = current_device();
     if (dev < 0)
         return -1;
+    if (w4a8 < 0 || w4a8 > 2)
+        return -1;
     const w4q::W4Mode mode = w4a8 ? w4q::W4Mode::A8 : w4q::W4Mode::A16;
     w4q::W4Plan plan;
-    if (!w4q::w4_plan((int)M, (int)N, (int)K, -1, sm_count(dev), mode, &plan))
+    if (!w4q::w4_plan((int)M, (int)N, (int)K, -1, sm_count(dev), mode, &plan, w4a8 == 2))
         return -1;
     // the cluster kernel alone; else the activation preparation (and counter
     // reset), the main kernel, and for the tensor-core kernel with split row

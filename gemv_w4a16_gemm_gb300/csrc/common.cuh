@@ -108,14 +108,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 #endif
 // Wait for the phase of `parity`, the thread sleeping in the instruction
 // (at most W4Q_SLEEP_NS per poll) instead of spinning, so waiting warps
-// leave the issue slots to the others; false after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity)
+// leave the issue slots to the others; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                unsigned long long limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_timer();
     while (!mbar_try_wait_sleep(bar, parity, W4Q_SLEEP_NS))
-        if (global_timer() - t0 > WAIT_LIMIT_NS)
+        if (global_timer() - t0 > limit_ns)
             return false;
     return true;
 }

@@ -819,9 +819,24 @@ WsLayout ws_layout(const W4Plan &pl, W4Mode mode)
 // takes about (waves of CTAs) x (super-blocks per CTA + 2) stage times, the
 // + 2 standing for each CTA's fixed part (activation preparation, ramp,
 // cluster reduction); ties go to the smaller split.
-#ifndef W4Q_CLUSTER_PATH
-#define W4Q_CLUSTER_PATH 0
-#endif
+// The measured split table (tune_splits.py): the fastest K split of listed
+// M <= 8 calls on a GPU with this many SMs.
+struct SplitEntry {
+    int sms, kind, M, N, K, split, ns;
+};
+const SplitEntry kSplitTable[] = {
+#include "split_table.inc"
+    {0, 0, 0, 0, 0, 0, 0}};
+
+// kind: 0 W4A16, 1 W4A8 with a scale per group, 2 W4A8 with a scale per row
+int table_split(int sms, int kind, int M, int N, int K)
+{
+    for (const SplitEntry &e : kSplitTable)
+        if (e.sms == sms && e.kind == kind && e.M == M && e.N == N && e.K == K)
+            return e.split;
+    return -1;
+}
+
 int cluster_choice(int M, int G, int KB, int sm_count)
 {
     const long long slots = 2LL * (sm_count > 0 ? sm_count : 1);
@@ -842,7 +857,8 @@ int cluster_choice(int M, int G, int KB, int sm_count)
 
 }  // namespace
 
-bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan)
+bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan,
+             bool act_row)
 {
     if (M < 1 || M > 64 || N < 1 || K < 256 || K % 256 != 0)
         return false;
@@ -869,9 +885,16 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     // library's own choice and explicit splits of 1..8 whenever the slice
     // of activations it keeps in shared memory fits; stream-K (split 0),
     // larger explicit splits and the longest K stay on the stream-K kernel.
-    if (!pl.umma && W4Q_CLUSTER_PATH) {
+    if (!pl.umma && split < 0) {
+        // a measured choice for this call, if the table has one
+        const int t = table_split(sm_count, mode == W4Mode::A16 ? 0 : (act_row ? 2 : 1), M, N, K);
+        if (t >= 0 && t <= pl.KB)
+            split = t;
+    }
+    if (!pl.umma) {
         const int C = split < 0 ? cluster_choice(M, pl.G, pl.KB, sm_count)
-                                : (split <= 8 && w4_cluster_ring(M, pl.KB, split) > 0 ? split : 0);
+                                : (split >= 1 && split <= 8 && w4_cluster_ring(M, pl.KB, split) > 0
+                                       ? split : 0);
         if (C > 0) {
             pl.cluster = C;
             pl.split = C;

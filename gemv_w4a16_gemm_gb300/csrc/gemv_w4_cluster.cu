@@ -78,11 +78,12 @@ __device__ __forceinline__ uint32_t cluster_rank()
 }
 
 // Barrier over every thread of every CTA of the cluster; shared-memory
-// writes before it are visible to the cluster's reads after it.
+// writes before it are visible to the cluster's reads after it.  (Not the
+// .aligned form: the producer warp's lanes reach it from divergent code.)
 __device__ __forceinline__ void cluster_sync()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // The shared::cluster address of this CTA's shared-memory address `addr` in
@@ -355,8 +356,10 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
         // ----------------------------------------------------- consumers
         for (int i = 0; i < S; ++i) {
             const int slot = i % R;
-            if (!W4Q_RING_WAIT(full0 + 8 * slot, (uint32_t)(i / R) & 1)) {
-                report_error(p.err, ERR_FULL_WAIT);
+            const bool got = W4Q_RING_WAIT(full0 + 8 * slot, (uint32_t)(i / R) & 1);
+            if (!__all_sync(0xffffffffu, got)) {  // the whole warp leaves together
+                if (lane == 0)
+                    report_error(p.err, ERR_FULL_WAIT);
                 break;
             }
             if (tile < p.T) {

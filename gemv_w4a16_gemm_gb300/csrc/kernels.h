@@ -38,7 +38,9 @@ enum class W4Mode { A16, A8, A8_DOTS };
 
 // Plan for these sizes (split: -1 = the library's choice, 0 = stream-K,
 // s >= 1 = fixed).  Returns false when the sizes or split are unsupported.
-bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan);
+// act_row: W4A8 with one activation scale per row (the split table keys it apart).
+bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan,
+             bool act_row = false);
 
 // Workspace bytes for a plan (partials + the W4A8 activation buffers).
 size_t w4_workspace_for(const W4Plan &plan, W4Mode mode);

@@ -51,6 +51,7 @@ SIGNATURES = {
     "w4a8_group_dots_rowscale": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, _P, _SZ, _P]),
     "w8_gemv": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "w4q_device_error": (_INT, [_U32P]),
+    "w4q_selftest_wait_expiry": (_INT, [ctypes.c_uint, _P]),
 }
 
 
@@ -118,8 +119,11 @@ def split_choice(M: int, N: int, K: int, group: int = GROUP) -> int:
     return int(lib().w4_split_choice(M, N, K, group))
 
 
-def kernel_launches(M: int, N: int, K: int, w4a8: bool = False, group: int = GROUP) -> int:
-    return int(lib().w4_kernel_launches(M, N, K, group, 1 if w4a8 else 0))
+def kernel_launches(M: int, N: int, K: int, w4a8=False, group: int = GROUP) -> int:
+    """Kernels one call launches: w4a8 False = W4A16, True or "group" = W4A8
+    with a scale per group of 32, "row" = W4A8 with a scale per row."""
+    mode = 2 if w4a8 == "row" else (1 if w4a8 else 0)
+    return int(lib().w4_kernel_launches(M, N, K, group, mode))
 
 
 def _workspace(M, N, K, group, split_k, workspace, device):

@@ -122,26 +122,32 @@ int w4_unpack_weights(const void *packed, int64_t N, int64_t K, int group,
                       uint8_t *q, void *scale_bf16, uint8_t *zero,
                       void *stream);
 
-/* Workspace bytes needed by w4a16_gemm and w4a8_gemm for these sizes on the
- * current device with the library's own split choice (0 if none is needed;
- * w4a8_gemm always needs some).  One buffer of this size serves both. */
+/* Workspace bytes needed by w4a16_gemm, w4a8_gemm and w4a8_gemm_rowscale
+ * for these sizes on the current device with the library's own split
+ * choice (0 if none is needed; a call on the cluster kernel, the usual case
+ * at M <= 8, needs none).  One buffer of this size serves all three. */
 size_t w4_workspace_bytes(int64_t M, int64_t N, int64_t K, int group);
 
 /* Same, for an explicit split_k (see w4a16_gemm_split); 0 if unsupported. */
 size_t w4_workspace_bytes_split(int64_t M, int64_t N, int64_t K, int group,
                                 int split_k);
 
-/* The split the library picks for these sizes on the current device:
- * 0 = balanced stream-K partition over all SMs, s >= 1 = fixed K split. */
+/* The split the library picks for a W4A16 call of these sizes on the
+ * current device: 0 = balanced stream-K partition over all SMs, s >= 1 =
+ * fixed K split (at M <= 8: s CTAs of one thread-block cluster per 128-row
+ * group, where the call fits the cluster kernel).  At M <= 8 the choice is
+ * the measured one of the library's split table when it lists the call for
+ * this GPU's SM count (tune_splits.py), else a cost model's. */
 int w4_split_choice(int64_t M, int64_t N, int64_t K, int group);
 
-/* Number of kernels one w4a16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1) call
- * with these sizes launches on the current device: a prologue (split-K
- * counter reset; W4A8: also the activation quantizer; W4A16 at M >= 9: the
- * tensor-core operand layout) and the main kernel (W4A16 at M <= 8 prepares
- * its activation operand itself); for W4A16 at M >= 9 with row groups split
- * over several CTAs, also the launch that sums their fp32 partials.  -1 when
- * the sizes are unsupported. */
+/* Number of kernels one call with these sizes launches on the current
+ * device, for w4a8 = 0 (w4a16_gemm), 1 (w4a8_gemm) or 2
+ * (w4a8_gemm_rowscale): 1 for a call on the cluster kernel (M <= 8, the
+ * activations prepared and the split-K partials summed inside it);
+ * otherwise a prologue (split-K counter reset; W4A8: also the activation
+ * quantizer; W4A16 at M >= 9: the tensor-core operand layout), the main
+ * kernel, and for W4A16 at M >= 9 with row groups split over several CTAs
+ * the launch that sums their fp32 partials.  -1 when unsupported. */
 int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
 
 /* out = x . dequant(packed)^T, W4A16.
@@ -151,7 +157,8 @@ int w4_kernel_launches(int64_t M, int64_t N, int64_t K, int group, int w4a8);
  *   workspace  device scratch of >= w4_workspace_bytes(M,N,K,group) bytes
  *              (may be NULL when that is 0); contents are clobbered.
  * Accumulates in fp32: for M <= 8 per group, sum_k (q - z) * x exactly in
- * the tensor core, then acc += s * sum; for M >= 9 the dequantized weight
+ * the tensor core, then acc += s * sum (and, where K is split over the CTAs
+ * of a cluster, the CTAs' sums added in rank order); for M >= 9 the dequantized weight
  * is rounded once to bf16 ((q - z) * s) and accumulated over all of K on
  * the tcgen05 tensor core.
  * out = bf16_RN(acc).  Defined by "test_int4_quantized_gemm.py", the
@@ -165,10 +172,14 @@ int w4a16_gemm(const void *x_bf16, const void *packed, void *out_bf16,
  * super-blocks (legal iff s <= K/256, "test_int4_quantized_gemm.py",
  * Int4QuantizedGemmRulesTest: one 256-wide K tile per split), partials are
  * summed in fixed order; split_k = 0 is the balanced stream-K partition.
- * The library's own choice (w4a16_gemm, see w4_split_choice) is stream-K,
- * except on the tensor-core path (M >= 9) with at most 4 super-blocks and
- * no more 256-row pairs than SMs, where it is 1 (whole K per CTA, no
- * partial-sum launch).  Illegal s returns W4Q_ERR_UNSUPPORTED. */
+ * At M <= 8, s in 1..8 runs on the cluster kernel (s CTAs per cluster,
+ * partials summed over distributed shared memory, no workspace) whenever
+ * the CTA's slice of prepared activations fits its shared memory, and on
+ * the stream-K kernel with a fixed split otherwise.  The library's own
+ * choice is described at w4_split_choice; on the tensor-core path (M >= 9)
+ * it is stream-K, or 1 (whole K per CTA, no partial-sum launch) with at
+ * most 4 super-blocks and no more 256-row pairs than SMs.  Illegal s
+ * returns W4Q_ERR_UNSUPPORTED. */
 int w4a16_gemm_split(const void *x_bf16, const void *packed, void *out_bf16,
                      int64_t M, int64_t N, int64_t K, int group, int split_k,
                      void *workspace, size_t workspace_bytes, void *stream);
@@ -206,7 +217,9 @@ int w4a16_gemm_noalloc(const void *x_bf16, const void *packed, void *out_bf16, i
  * case of Int4QuantizedGemmPrecisionTest ("test_int4_quantized_gemm.py")
  * fails with one scale per row.
  * Arguments as w4a16_gemm with 1 <= M <= 8 (the pages' W4A8 buckets are
- * 1..4); the workspace is required (it holds the prepared activations). */
+ * 1..4); the workspace is needed only where w4_workspace_bytes says so (the
+ * stream-K kernel keeps the prepared activations there; the cluster kernel
+ * keeps them in shared memory). */
 int w4a8_gemm(const void *x_bf16, const void *packed, void *out_bf16,
               int64_t M, int64_t N, int64_t K, int group, void *workspace,
               size_t workspace_bytes, void *stream);
@@ -278,8 +291,20 @@ int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16,
 
 /* Read and clear the device-side error word of the current device (set by
  * a kernel whose bounded wait on a barrier ran out).  Synchronizes the
- * device.  *code receives the word (0 = no error). */
+ * device.  *code receives the word (0 = no error): bit 0 a consumer's wait
+ * for a full stage, bit 1 the producer's wait for a free stage, bit 2 the
+ * final wait for copies in flight.  Returns W4Q_ERR_DEVICE when the word
+ * was not 0.  After such an error the outputs of the calls since the last
+ * read are unspecified. */
 int w4q_device_error(uint32_t *code);
+
+/* Self-test of that protocol (the pages have no counterpart): launches one
+ * kernel on `stream` whose single waiting thread waits, with the library's
+ * bounded sleeping wait, on a shared-memory barrier phase that nothing
+ * completes, gives up after limit_us microseconds (1..100000) and sets bit
+ * 0 of the error word, as a kernel of the library does when its wait runs
+ * out.  Nothing faults and the context stays usable.  For tests. */
+int w4q_selftest_wait_expiry(unsigned limit_us, void *stream);
 
 #ifdef __cplusplus
 }

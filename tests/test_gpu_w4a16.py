@@ -92,11 +92,12 @@ def test_every_runtime_m_up_to_64(cuda):
 
 
 def test_workspace_too_small_is_rejected(cuda):
-    # w4_workspace_bytes covers both W4A16 and W4A8 (the larger, with the
-    # int8 activation buffers); a buffer 16 bytes short fails W4A8, and a
-    # 16-byte buffer fails W4A16.
+    # The stream-K partition (split 0) needs a workspace: w4_workspace_bytes
+    # covers both W4A16 and W4A8 (the larger, with the int8 activation
+    # buffers); a buffer 16 bytes short fails W4A8, and a 16-byte buffer
+    # fails W4A16 (its split-K counters and partials do not fit).
     N, K, M = 8448, 6656, 4
-    need = w4q.workspace_bytes(M, N, K)
+    need = w4q.workspace_bytes(M, N, K, split_k=0)
     assert need > 0
     W = workloads.w4_weight(N, K)
     packed = w4q.w4_pack_weights(W.to(cuda))
@@ -104,12 +105,10 @@ def test_workspace_too_small_is_rejected(cuda):
     out = torch.full((M, N), 3.0, dtype=torch.bfloat16, device=cuda)
     small = torch.empty(need - 16, dtype=torch.uint8, device=cuda)
     with pytest.raises(w4q.W4QError) as e:
-        w4q.w4a8_gemm(x, packed, N, K, workspace=small, out=out)
+        w4q.w4a8_gemm(x, packed, N, K, split_k=0, workspace=small, out=out)
     assert e.value.status == 4
-    # W4A16 at this shape splits row groups over CTAs: its split-K counters
-    # and partials do not fit in 16 bytes
     with pytest.raises(w4q.W4QError) as e:
-        w4q.w4a16_gemm(x, packed, N, K, workspace=small[:16], out=out)
+        w4q.w4a16_gemm(x, packed, N, K, split_k=0, workspace=small[:16], out=out)
     assert e.value.status == 4
     assert torch.all(out == 3.0)
 
@@ -193,7 +192,20 @@ def test_partition_choice_and_launch_count(cuda):
     # launch where row-group pairs are split over CTAs.
     assert w4q.split_choice(16, 39936, 6656) == 0
     assert w4q.kernel_launches(16, 39936, 6656) == 3
-    # The mma.sync path (M <= 8) keeps stream-K with few super-blocks too
-    # (its split-K sum is inside the main kernel).
-    assert w4q.split_choice(4, 1536, 512) == 0
-    assert w4q.kernel_launches(4, 1536, 512) == 2
+    # M <= 8: a cluster split (1..8 CTAs per 128-row group) is one launch
+    # with no workspace; stream-K (0) is a prologue and the main kernel.
+    for (N, K) in ((1536, 512), (256, 6656), (8448, 6656), (6656, 4096), (6656, 19968),
+                   (39936, 6656), (300, 512)):
+        for M in (1, 2, 3, 4, 8):
+            for kind in (False, "group", "row"):
+                if kind and M > 8:
+                    continue
+                c = w4q.split_choice(M, N, K)
+                assert 0 <= c <= 8, (N, K, M, c)
+                n = w4q.kernel_launches(M, N, K, kind)
+                if kind is False:
+                    assert n == (1 if c >= 1 else 2), (N, K, M, c, n)
+                    if c >= 1:
+                        assert w4q.workspace_bytes(M, N, K, split_k=c) == 0
+                else:
+                    assert n in (1, 2), (N, K, M, kind, n)

@@ -48,6 +48,7 @@ def test_group_dots_bit_exact(cuda, N, K, M):
     W, q, s, z = quantized(N, K, seed=N ^ K ^ 5)
     packed = w4q.w4_pack_weights(W.to(cuda))
     x = workloads.activation(M, K, seed=M + 23)
+    x[0, K - 3] = 40.0   # row 0's max sits in the last K slice (the last CTA of a cluster)
     D = w4q.w4a8_group_dots_rowscale(x.to(cuda), packed, N, K).cpu().numpy()
     xq, sx = oracle.act_quant_row(x, K)
     ref = oracle.w4a8_group_dots(xq, q, z)
@@ -88,8 +89,24 @@ def test_model_shapes(cuda, N, K):
 
 def test_every_legal_split_matches(cuda):
     N, K = 256, 4096
-    for split in (0, 1, 2, 4, 16):
+    for split in (0, 1, 2, 3, 4, 5, 7, 8, 16):
         _check(cuda, N, K, (1, 4), split_k=split, seed_w=93)
+
+
+def test_row_max_in_another_slice_of_the_cluster(cuda):
+    # per-row scale with the row's max in a different K slice for each row,
+    # under every cluster split: the slices' maxima must be combined
+    N, K = 384, 2048
+    W, q, s, z = quantized(N, K, seed=94)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    x = workloads.activation(4, K, seed=95)
+    for m, k in enumerate((5, 700, 1300, K - 1)):
+        x[m, k] = 60.0 * (1 if m % 2 else -1)
+    xq, sx = oracle.act_quant_row(x, K)
+    ref8 = oracle.w4a8_row(xq, sx, q, s, z)
+    for split in (1, 2, 3, 5, 8):
+        out = w4q.w4a8_gemm_rowscale(x.to(cuda), packed, N, K, split_k=split)
+        assert_close(out, ref8, "split %d" % split)
 
 
 def test_zero_rows_and_more_than_eight_rows(cuda):
