@@ -24,18 +24,22 @@
 //             fp32, with sx = fp32(max|x| / 127) over a group of 32 or over
 //             the whole row; x' = xq * 2^121 (2^117 upper), X' = 2^-12 *
 //             sum xq, and sx * 2^12 per group.  The row scale needs the max
-//             over all of K: each CTA reduces its slice, the cluster
-//             exchanges the C partial maxima through distributed shared
-//             memory, and every CTA takes the max of them.
+//             over all of K: each CTA reduces its slice and sends its maxima
+//             to every other CTA of the cluster (asynchronous stores into
+//             their shared memory that count on their barriers); each CTA
+//             takes the max of the C slices' values.
 //  * Eight consumer warps each own one 16-row tile and run the same stage
 //    arithmetic as the stream-K kernel (w4_stage.cuh): bf16 m16n8k16 MMAs on
 //    the masked nibbles, exact per-group dots, the fp32 scale / zero update.
-//  * Split-K reduction: each CTA leaves its 128 x M fp32 sums in its shared
-//    memory; after a cluster barrier, CTA r sums the C CTAs' values of rows
-//    [r*128/C, (r+1)*128/C) over distributed shared memory in rank order
-//    (fixed order: the result does not depend on timing) and writes them
-//    as bf16.  A second cluster barrier keeps every CTA's shared memory
-//    alive until its peers have read it.
+//  * Split-K reduction: every CTA of rank r > 0 sends its 128 x MP fp32 sums
+//    into slot r - 1 of rank 0's shared memory with asynchronous stores
+//    whose bytes count on a barrier of rank 0, and leaves; rank 0 waits for
+//    all the bytes, adds the C ranks' sums in rank order (fixed order: the
+//    result does not depend on timing) and writes them as bf16.  The only
+//    wait on other CTAs is rank 0's, on data already sent.  The barriers
+//    that receive remote bytes are initialised before a cluster-wide
+//    arrive (relaxed) that every thread passes at the start, and each CTA
+//    waits on that cluster barrier before its first remote store.
 //  * Every ring wait is bounded (one second of %globaltimer): on expiry the
 //    kernel sets a bit in the error word, still passes the cluster barriers
 //    (every thread reaches them on every path), drains its copies and
@@ -77,13 +81,27 @@ __device__ __forceinline__ uint32_t cluster_rank()
     return r;
 }
 
-// Barrier over every thread of every CTA of the cluster; shared-memory
-// writes before it are visible to the cluster's reads after it.  (Not the
-// .aligned form: the producer warp's lanes reach it from divergent code.)
-__device__ __forceinline__ void cluster_sync()
+// The split form: arrive (relaxed: nothing before it needs publishing
+// beyond the barrier initialisation, which its fence releases) at the
+// start, wait before the first remote operation.
+__device__ __forceinline__ void cluster_arrive_relaxed()
 {
-    asm volatile("barrier.cluster.arrive.release;\n\t"
-                 "barrier.cluster.wait.acquire;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 16 bytes from registers into another CTA's shared memory (shared::cluster
+// addresses of the data and of that CTA's barrier), counted on the barrier
+// as transaction bytes.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+                 : "memory");
 }
 
 // The shared::cluster address of this CTA's shared-memory address `addr` in
@@ -95,30 +113,17 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank)
     return d;
 }
 
-__device__ __forceinline__ float ld_peer_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // ----------------------------------------------------------- smem layout
 
 struct CLayout {
-    int ring, xr, xs, xg, red, rowmax, zero, bars, total;
+    int ring, xr, xs, xg, red, recv, rowmax, zero, bars, total;
 };
 
 // [ring: R x 19456][x': smax x MP x 528][X': smax x MP x 32][factors:
-// smax x MP x 32][partial sums: 128 x MP f32][row maxima: 8 u32][16 zero
-// bytes][barriers: 2R x 8]
-__host__ __device__ inline CLayout c_layout(int mp, int smax, int R)
+// smax x MP x 32][partial sums: 128 x MP f32][received sums (rank 0):
+// (C-1) x 128 x MP f32][row maxima: own + received, C x 8 u32][16 zero
+// bytes][barriers: 2R ring + received sums + received maxima, x 8]
+__host__ __device__ inline CLayout c_layout(int mp, int smax, int R, int C)
 {
     CLayout L;
     int o = 0;
@@ -132,12 +137,14 @@ __host__ __device__ inline CLayout c_layout(int mp, int smax, int R)
     o += smax * mp * SROW;
     L.red = o;
     o += GROUP_ROWS * mp * 4;
+    L.recv = o;
+    o += (C - 1) * GROUP_ROWS * mp * 4;
     L.rowmax = o;
-    o += 32;
+    o += C * 32;
     L.zero = o;
     o += 16;
     L.bars = o;
-    o += 2 * R * 8;
+    o += (2 * R + 2) * 8;
     L.total = (o + 127) / 128 * 128;
     return L;
 }
@@ -208,11 +215,13 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
     const int R = p.R;
 
     extern __shared__ __align__(128) uint8_t smem[];
-    const CLayout L = c_layout(MP, p.smax, R);
+    const CLayout L = c_layout(MP, p.smax, R, p.C);
     uint8_t *xr = smem + L.xr, *xs = smem + L.xs, *xg = smem + L.xg;
     float *red = reinterpret_cast<float *>(smem + L.red);
     uint32_t *rowmax = reinterpret_cast<uint32_t *>(smem + L.rowmax);
     const uint32_t full0 = smem_addr(smem + L.bars), empty0 = full0 + 8 * R;
+    const uint32_t recv_bar = empty0 + 8 * R;  // rank 0: the other ranks' sums have landed
+    const uint32_t max_bar = recv_bar + 8;     // ROW: the other ranks' row maxima have landed
     const uint32_t zrow = smem_addr(smem + L.zero);
 
     // hardware warp 0 produces (the schedulers favour low warp ids); 1..8
@@ -229,12 +238,20 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, WARPS);
         }
+        mbar_init(recv_bar, 1);
+        mbar_init(max_bar, 1);
+        // the bytes the other ranks will send (the phase completes when they
+        // have all landed; a rank's bytes may arrive before this)
+        if (!DOTS && rank == 0)
+            mbar_arrive_expect_tx(recv_bar, (uint32_t)((p.C - 1) * GROUP_ROWS * MP * 4));
+        if (ROW)
+            mbar_arrive_expect_tx(max_bar, (uint32_t)((p.C - 1) * 32));
         fence_barrier_init();
     }
-    // zero: the 16-byte zero row, the row maxima, and the activation rows
-    // m >= M of every stage (read by the MMAs, never stored)
+    // zero: the 16-byte zero row, this rank's row maxima, and the activation
+    // rows m >= M of every stage (read by the MMAs, never stored)
     if (threadIdx.x < 8)
-        rowmax[threadIdx.x] = 0u;
+        rowmax[8 * rank + threadIdx.x] = 0u;  // this rank's slot
     if (threadIdx.x == 8)
         *reinterpret_cast<uint4 *>(smem + L.zero) = make_uint4(0u, 0u, 0u, 0u);
     {
@@ -255,6 +272,7 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
         }
     }
     __syncthreads();
+    cluster_arrive_relaxed();  // every CTA's barriers are initialised (waited on below)
     pdl_launch_dependents();  // the next kernel on the stream may launch and prefetch
 
     // -------------------------------------------- weight prefetch (no wait)
@@ -301,18 +319,28 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
                     if (m < p.M) {
                         *reinterpret_cast<uint4 *>(xr + (s * MP + m) * XROW + 16 * lane) = raw[m];
                         if (lane == 0)
-                            atomicMax(&rowmax[m], h);
+                            atomicMax(&rowmax[8 * rank + m], h);
                     }
                 }
             }
-            cluster_sync();  // every CTA's slice maxima are written
+            __syncthreads();  // this CTA's slice maxima are complete
+            cluster_wait();   // every CTA's barriers are initialised
+            // send them into slot `rank` of every other CTA's row maxima
+            if (threadIdx.x < p.C && threadIdx.x != rank) {
+                const uint32_t *own = rowmax + 8 * rank;
+                const uint32_t dst = peer_addr(smem_addr(own), threadIdx.x);
+                const uint32_t bar = peer_addr(max_bar, threadIdx.x);
+                st_async_v4(dst, make_uint4(own[0], own[1], own[2], own[3]), bar);
+                st_async_v4(dst + 16, make_uint4(own[4], own[5], own[6], own[7]), bar);
+            }
+            if (p.C > 1 && !mbar_wait_sleep(max_bar, 0u))
+                report_error(p.err, ERR_FULL_WAIT);
             // the row's max over the C slices (magnitudes order as bf16 bits)
-            const uint32_t base = smem_addr(rowmax);
 #pragma unroll
             for (int m = 0; m < MP; ++m) {
                 uint32_t h = 0u;
                 for (int c = 0; c < p.C; ++c)
-                    h = max(h, ld_peer_u32(peer_addr(base + 4 * m, (uint32_t)c)));
+                    h = max(h, rowmax[8 * c + m]);
                 arow[m] = __uint_as_float(h << 16);
             }
         }
@@ -408,24 +436,32 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
     }
 
     // ---------------------------------------------- split-K over the cluster
-    cluster_sync();  // every CTA's partial sums are in its shared memory
+    if constexpr (!ROW)
+        cluster_wait();  // every CTA's barriers are initialised (ROW waited above)
     if (!DOTS) {
-        const int C = p.C;
-        const int r0 = (int)(rank * GROUP_ROWS / C), r1 = (int)((rank + 1) * GROUP_ROWS / C);
-        const int nr = r1 - r0;
-        const uint32_t rbase = smem_addr(red);
-        for (int t = threadIdx.x; t < nr * p.M; t += THREADS) {
-            const int row = r0 + t % nr, m = t / nr;
-            const uint32_t a = rbase + 4 * (row * MP + m);
-            float v = ld_peer_f32(peer_addr(a, 0u));
-            for (int c = 1; c < C; ++c)
-                v += ld_peer_f32(peer_addr(a, (uint32_t)c));
-            const int n = g * GROUP_ROWS + row;
-            if (n < p.N)
-                p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
+        __syncthreads();  // this CTA's 128 x MP sums are complete
+        const int n4 = GROUP_ROWS * MP / 4;  // 16-byte pieces of them
+        if (rank != 0) {
+            // send them into slot rank - 1 of rank 0's received sums, and go
+            const uint32_t dst = peer_addr(smem_addr(smem + L.recv) + (rank - 1) * (n4 * 16), 0u);
+            const uint32_t bar = peer_addr(recv_bar, 0u);
+            for (int i = threadIdx.x; i < n4; i += THREADS)
+                st_async_v4(dst + 16 * i, reinterpret_cast<const uint4 *>(red)[i], bar);
+        } else {
+            if (p.C > 1 && !mbar_wait_sleep(recv_bar, 0u))
+                report_error(p.err, ERR_FULL_WAIT);
+            const float *recv = reinterpret_cast<const float *>(smem + L.recv);
+            for (int t = threadIdx.x; t < GROUP_ROWS * p.M; t += THREADS) {
+                const int row = t % GROUP_ROWS, m = t / GROUP_ROWS;
+                float v = red[row * MP + m];
+                for (int c = 1; c < p.C; ++c)
+                    v += recv[(c - 1) * GROUP_ROWS * MP + row * MP + m];
+                const int n = g * GROUP_ROWS + row;
+                if (n < p.N)
+                    p.out[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
+            }
         }
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 
     // Drain: every issued stage's copy must have landed before the shared
     // memory goes away (only the error path can leave one pending).
@@ -498,7 +534,7 @@ int w4_cluster_ring(int M, int KB, int C)
         return 0;
     const int smax = (KB + C - 1) / C;
     for (int R = 4; R >= 2; --R)
-        if (c_layout(mp_of(M), smax, R).total <= CTA_SMEM_MAX)
+        if (c_layout(mp_of(M), smax, R, C).total <= CTA_SMEM_MAX)
             return R;
     return 0;
 }
@@ -525,7 +561,7 @@ cudaError_t launch_w4_cluster(const W4Plan &plan, W4Mode mode, bool act_row, con
     if (p.R == 0)
         return cudaErrorInvalidValue;
     const int mp = mp_of(plan.M);
-    const int smem = c_layout(mp, p.smax, p.R).total;
+    const int smem = c_layout(mp, p.smax, p.R, p.C).total;
     if (mode == W4Mode::A16)
         return dispatch_mp<W4Mode::A16, false>(p, mp, smem, stream);
     if (mode == W4Mode::A8)
