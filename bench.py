@@ -111,13 +111,17 @@ def call_label(kind, N, K, M):
     return "%s N=%d K=%d M=%d" % (kind, N, K, M)
 
 
-def kernel_name(kind, M):
+def kernel_name(kind, M, launches=None):
+    """The call's main kernel; `launches` (the library's launch count for the
+    call) tells the one-launch cluster kernel from the stream-K kernel."""
     if kind == "w8":
         return "w8_kernel<M=%d>" % M
     if kind == "w4a16" and M >= 9:
         return "w4_umma_kernel<NP=%d>" % ((M + 15) // 16 * 16)
-    nb = 1 if M <= 8 else (2 if M <= 16 else (4 if M <= 32 else 8))
-    return "w4_kernel<NB=%d,%s>" % (nb, "A16" if kind == "w4a16" else "A8")
+    mode = "A16" if kind == "w4a16" else "A8"
+    if launches == 1:
+        return "w4_cluster_kernel<%s>" % mode
+    return "w4_kernel<NB=1,%s>" % mode
 
 
 # ------------------------------------------------------------------- clocks
@@ -297,8 +301,10 @@ def measure_calls(suite, reps=3):
             b.synchronize()
             times.append(a.elapsed_time(b) * 1e3 / R)
         us = statistics.median(times[1:])
+        launches = None if kind == "w8" else suite.w4q.kernel_launches(
+            M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
         res.append(dict(call=call_label(kind, N, K, M), kind=kind, N=N, K=K, M=M,
-                        kernel=kernel_name(kind, M), us=us,
+                        kernel=kernel_name(kind, M, launches), us=us,
                         weight_gbs=weight_bytes(kind, N, K) / us / 1e3,
                         alg_gbs=algorithmic_bytes(kind, N, K, M) / us / 1e3))
         del g

@@ -69,6 +69,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "timeline.cuh"
 #include "w4_stage.cuh"
 
 // Ring waits of this file: sleeping in mbarrier.try_wait (the default) or
@@ -190,6 +191,8 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0)
+        W4Q_STAMP(10);
     pdl_launch_dependents();  // the next call's preparation may launch and wait
 
     // stage i processes unit u0 + i = (g, b); both sides step (g, b) along
@@ -250,6 +253,8 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
             for (int i = 0; i < first; ++i)
                 issue_w(i);
             pdl_wait();  // x may come from the previous kernel
+            if (lane == 0)
+                W4Q_STAMP(11);
 #pragma unroll
             for (int d = 0; d < PD; ++d)
                 load_into(raw[d]);
@@ -318,6 +323,7 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 }
             }
             pdl_wait();  // the activations come from act_prep, launched just before
+            W4Q_STAMP(11);
             int xb = b_first;
             for (int i = 0; i < first; ++i) {
                 issue_x(i, xb);
@@ -478,6 +484,8 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 ok = false;
                 break;
             }
+            if (i == 0 && lane == 0 && warp == 0)
+                W4Q_STAMP(13);
             const int tile = g * WARPS + warp;
             if (tile < p.T)
             {
@@ -500,11 +508,17 @@ __global__ void __launch_bounds__(THREADS, (NB <= 4 ? 2 : 1)) w4_kernel(const Pa
                 ++g;
             }
         }
+        if (lane == 0 && warp == 0)
+            W4Q_STAMP(14);
         if (ok && n_iter > 0)
             flush(cur_g);
+        if (lane == 0 && warp == 0)
+            W4Q_STAMP(15);
     }
 
     __syncthreads();
+    if (threadIdx.x == 0)
+        W4Q_STAMP(16);
     // Drain: every issued stage's copies must have landed before the CTA's
     // shared memory goes away (only the error path can leave some pending).
     if (warp == WARPS && lane == 0) {
@@ -529,8 +543,12 @@ constexpr int PREP_CHUNK = PREP_THREADS * 8;  // columns one act_prep CTA transf
 __global__ void __launch_bounds__(PREP_THREADS) splitk_reset_kernel(unsigned *__restrict__ counters,
                                                                     int ncounters)
 {
+    if (threadIdx.x == 0)
+        W4Q_STAMP(1);
     pdl_launch_dependents();  // the main kernel may start streaming weights
     pdl_wait();               // the previous kernel may still use these counters
+    if (threadIdx.x == 0)
+        W4Q_STAMP(2);
     for (int i = blockIdx.x * PREP_THREADS + threadIdx.x; i < ncounters; i += gridDim.x * PREP_THREADS)
         counters[i] = 0u;
 }
@@ -572,8 +590,12 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     float *__restrict__ xsum, float *__restrict__ gscale, unsigned *__restrict__ counters,
     int ncounters)
 {
+    if (threadIdx.x == 0)
+        W4Q_STAMP(4);
     pdl_launch_dependents();  // the main kernel may start streaming weights
     pdl_wait();               // x (and this workspace) may belong to the previous kernel
+    if (threadIdx.x == 0)
+        W4Q_STAMP(5);
     const int nblk = gridDim.x * gridDim.y;
     const int bid = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = bid * PREP_THREADS + threadIdx.x; i < ncounters; i += nblk * PREP_THREADS)
@@ -1027,3 +1049,5 @@ cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *
 }
 
 }  // namespace w4q
+
+W4Q_STAMP_READER(w4q_timeline_read_w4)

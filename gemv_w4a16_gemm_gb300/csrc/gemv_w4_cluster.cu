@@ -48,6 +48,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "timeline.cuh"
 #include "w4_stage.cuh"
 
 #ifdef W4Q_SPIN_WAITS
@@ -273,6 +274,8 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
     }
     __syncthreads();
     cluster_arrive_relaxed();  // every CTA's barriers are initialised (waited on below)
+    if (threadIdx.x == 0)
+        W4Q_STAMP(20);
     pdl_launch_dependents();  // the next kernel on the stream may launch and prefetch
 
     // -------------------------------------------- weight prefetch (no wait)
@@ -291,6 +294,8 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
 
     // ------------------------------------- the slice's activation operand
     pdl_wait();  // x may come from the kernel launched before this one
+    if (threadIdx.x == 0)
+        W4Q_STAMP(21);
     if constexpr (A16) {
         for (int s = hw_warp; s < S; s += WARPS + 1) {
             uint4 raw[MP];
@@ -361,6 +366,8 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
         }
     }
     __syncthreads();  // the slice's activation operand is complete
+    if (threadIdx.x == 0)
+        W4Q_STAMP(22);
 
     float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
     const int tile = g * WARPS + warp;
@@ -435,6 +442,8 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
         }
     }
 
+    if (threadIdx.x == 32)
+        W4Q_STAMP(23);
     // ---------------------------------------------- split-K over the cluster
     if constexpr (!ROW)
         cluster_wait();  // every CTA's barriers are initialised (ROW waited above)
@@ -463,6 +472,8 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
         }
     }
 
+    if (threadIdx.x == 0)
+        W4Q_STAMP(25);
     // Drain: every issued stage's copy must have landed before the shared
     // memory goes away (only the error path can leave one pending).
     if (warp == WARPS && lane == 0) {
@@ -572,3 +583,5 @@ cudaError_t launch_w4_cluster(const W4Plan &plan, W4Mode mode, bool act_row, con
 }
 
 }  // namespace w4q
+
+W4Q_STAMP_READER(w4q_timeline_read_cluster)

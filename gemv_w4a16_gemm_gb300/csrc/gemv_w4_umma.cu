@@ -60,6 +60,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
+#include "timeline.cuh"
 
 namespace w4q {
 
@@ -226,6 +227,8 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_slot;
+    if (threadIdx.x == 0)
+        W4Q_STAMP(40);
 
     if (warp == 0) {
         // ----------------------------------------------- producer of the codes
@@ -266,6 +269,7 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
         if (lane == 0 && n_iter > 0) {
             const uint64_t pol_x = policy_evict_last();
             pdl_wait();  // x comes from act_prep, launched just before
+            W4Q_STAMP(41);
             int b = b_first, issued = 0;
             for (int i = 0; i < n_iter; ++i) {
                 const int slot = i % SX;
@@ -512,6 +516,8 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
     // The fixup launch may start once every CTA is here (it waits for the
     // grid's completion before reading partials); triggering any earlier
     // would park its blocks, waiting, beside the dequant warps.
+    if (threadIdx.x == 0)
+        W4Q_STAMP(42);
     pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();
@@ -530,8 +536,12 @@ __global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 
                                                             int M, int K, int NP,
                                                             uint8_t *__restrict__ xs)
 {
+    if (threadIdx.x == 0 && blockIdx.x == 0)
+        W4Q_STAMP(44);
     pdl_launch_dependents();  // the main kernel may start streaming weights
     pdl_wait();               // x (and this workspace) may belong to the previous kernel
+    if (threadIdx.x == 0 && blockIdx.x == 0)
+        W4Q_STAMP(45);
     const int tid = blockIdx.x * blockDim.x + threadIdx.x;
     const long long pieces = (long long)(K / 64) * NP * 4;
     if (tid >= pieces)
@@ -563,6 +573,8 @@ constexpr int UT_FIX_ROWS = 8;
 __global__ void __launch_bounds__(UT_PAIR_ROWS) umma_fixup_kernel(const UParams p)
 {
     pdl_wait();
+    if (threadIdx.x == 0)
+        W4Q_STAMP(47);
     const int gp = blockIdx.x, m0 = blockIdx.y * UT_FIX_ROWS, row = threadIdx.x;
     const long long gb = (long long)gp * p.KB, ge = gb + p.KB;
     const int cf = ut_range_owner(p, gb), cl = ut_range_owner(p, ge - 1);
@@ -710,3 +722,5 @@ cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed
 }
 
 }  // namespace w4q
+
+W4Q_STAMP_READER(w4q_timeline_read_umma)

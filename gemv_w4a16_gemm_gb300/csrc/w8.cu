@@ -7,7 +7,7 @@
 // once, keeps x resident, accumulates in fp32 and applies the scale at the
 // end.  This kernel is a new GB300 design with the same arithmetic.)
 //
-// Design (one CTA per SM: 16 consumer warps + 1 producer warp):
+// Design (one CTA per SM and call: 16 consumer warps + 1 producer warp):
 //  * CTA c owns a contiguous range of whole rows; those rows are one
 //    contiguous stretch of W, streamed through a shared-memory ring by 1-D
 //    bulk copies (TMA engine, L2 evict-first), RW rows per stage (RW fixed
@@ -23,6 +23,7 @@
 //    once to bf16.
 #include "common.cuh"
 #include "kernels.h"
+#include "timeline.cuh"
 
 // Ring waits of this file: sleeping in mbarrier.try_wait (the default) or
 // spinning on it.
@@ -38,7 +39,6 @@ namespace {
 
 constexpr int CWARPS = 16;                  // consumer warps
 constexpr int THREADS = (CWARPS + 1) * 32;  // + producer warp
-constexpr int STAGES = 5;
 constexpr int STAGE_BYTES = 32768;
 constexpr int MAX_ROWS = 64;                // rows per CTA
 constexpr int LANE_SPAN = CWARPS * 32 * 16; // bytes of a row covered per lane chunk
@@ -52,9 +52,13 @@ struct W8Params {
     int N, K, P;
 };
 
-template <int M, int CH, int RW>
-__global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
+// ST ring stages.  With 3 (M = 1) a CTA fits twice on an SM, so the next
+// call's CTA on the same SM starts, and streams its first stages, while
+// this one is still running; with 5 it holds a deeper ring alone.
+template <int M, int CH, int RW, int ST>
+__global__ void __launch_bounds__(THREADS, (ST <= 3 ? 2 : 1)) w8_kernel(const W8Params p)
 {
+    constexpr int STAGES = ST;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     float *red = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES);  // [CWARPS][MAX_ROWS][M]
@@ -75,6 +79,8 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
         fence_barrier_init();
     }
     __syncthreads();
+    if (threadIdx.x == 0)
+        W4Q_STAMP(30);
     pdl_launch_dependents();  // the next call's preparation may launch and wait
 
     int issued = 0;
@@ -99,6 +105,8 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
         }
     } else {
         pdl_wait();  // x may come from the kernel launched before this one
+        if (warp == 0 && lane == 0)
+            W4Q_STAMP(31);
         // activations of this lane's columns, fp32, for the whole kernel
         float xr[CH][16][M];
 #pragma unroll
@@ -181,6 +189,8 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0)
+        W4Q_STAMP(32);
     for (int i = threadIdx.x; i < rows * M; i += THREADS) {
         const int row = i / M, m = i % M;
         float s = 0.f;
@@ -200,11 +210,11 @@ __global__ void __launch_bounds__(THREADS, 1) w8_kernel(const W8Params p)
     }
 }
 
-template <int M, int CH, int RW>
+template <int M, int CH, int RW, int ST>
 cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
 {
-    const int smem = STAGES * STAGE_BYTES + CWARPS * MAX_ROWS * M * 4 + 2 * STAGES * 8;
-    cudaError_t e = cudaFuncSetAttribute(w8_kernel<M, CH, RW>,
+    const int smem = ST * STAGE_BYTES + CWARPS * MAX_ROWS * M * 4 + 2 * ST * 8;
+    cudaError_t e = cudaFuncSetAttribute(w8_kernel<M, CH, RW, ST>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
@@ -220,7 +230,7 @@ cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w8_kernel<M, CH, RW>, p);
+    return cudaLaunchKernelEx(&cfg, w8_kernel<M, CH, RW, ST>, p);
 }
 
 }  // namespace
@@ -251,14 +261,16 @@ cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *
     p.P = (N + per_cta - 1) / per_cta;
     const int ch = (K + LANE_SPAN - 1) / LANE_SPAN;  // 1: K <= 8192 (4 rows/stage), 2: <= 16384
     switch (M * 4 + ch) {
-    case 1 * 4 + 1: return launch_t<1, 1, 4>(p, stream);
-    case 1 * 4 + 2: return launch_t<1, 2, 2>(p, stream);
-    case 2 * 4 + 1: return launch_t<2, 1, 4>(p, stream);
-    case 2 * 4 + 2: return launch_t<2, 2, 2>(p, stream);
-    case 3 * 4 + 1: return launch_t<3, 1, 2>(p, stream);
-    case 4 * 4 + 1: return launch_t<4, 1, 2>(p, stream);
+    case 1 * 4 + 1: return launch_t<1, 1, 4, 3>(p, stream);
+    case 1 * 4 + 2: return launch_t<1, 2, 2, 5>(p, stream);
+    case 2 * 4 + 1: return launch_t<2, 1, 4, 5>(p, stream);
+    case 2 * 4 + 2: return launch_t<2, 2, 2, 5>(p, stream);
+    case 3 * 4 + 1: return launch_t<3, 1, 2, 5>(p, stream);
+    case 4 * 4 + 1: return launch_t<4, 1, 2, 5>(p, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace w4q
+
+W4Q_STAMP_READER(w4q_timeline_read_w8)
