@@ -19,6 +19,11 @@ header for the readings taken where the pages are silent):
   workload.
 * w8 -- "gpt-fast issue #114", WeightOnlyInt8Linear.forward.
 * pack_w4 / unpack_w4 -- this library's packed layout (no page counterpart).
+* quantize_w4c / dequant_w4c / pack_w4c / unpack_w4c / w4a16c -- the compact
+  metadata of "test_int4_quantized_gemm.py"'s CudaCoalescedInt4Tensor (uint8
+  scale and zero_point codes per group, float16 scale_step and
+  zero_point_step per row), read as code x step for both (the page prints
+  no dequant formula); the packed form is this library's own.
 """
 from __future__ import annotations
 
@@ -76,6 +81,12 @@ def _load():
                 "oracle_act_quant_row": [P, I, I, P, P],
                 "oracle_w4a8_row": [P, P, P, P, P, I, I, I, I, I, P],
                 "oracle_w8": [P, P, P, I, I, I, I, I, P],
+                "oracle_quantize_w4c": [P, I, I, P, P, P, P],
+                "oracle_dequant_w4c": [P, P, P, P, I, I, P],
+                "oracle_packed_bytes_c": [I, I],
+                "oracle_pack_w4c": [P, P, P, P, I, I, P],
+                "oracle_unpack_w4c": [P, I, I, P, P, P, P],
+                "oracle_w4a16c": [P, P, P, P, P, I, I, I, I, I, P],
                 "oracle_set_threads": [ctypes.c_int],
             }
             for name, args in sig.items():
@@ -83,6 +94,7 @@ def _load():
                 fn.argtypes = args
                 fn.restype = None
             lib.oracle_packed_bytes.restype = I
+            lib.oracle_packed_bytes_c.restype = I
             lib.oracle_set_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -225,3 +237,58 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16) to float64."""
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- compact
+
+def quantize_w4c(W_bf16, N: int, K: int):
+    """bf16 [N,K] -> (q u8 [N,K], sc u8 [N,K/32], zc u8 [N,K/32], steps fp16-bits u16 [N,2])."""
+    W = _u16(W_bf16).reshape(N, K)
+    q = np.empty((N, K), np.uint8)
+    sc = np.empty((N, K // GROUP), np.uint8)
+    zc = np.empty((N, K // GROUP), np.uint8)
+    steps = np.empty((N, 2), np.uint16)
+    _load().oracle_quantize_w4c(_ptr(W), N, K, _ptr(q), _ptr(sc), _ptr(zc), _ptr(steps))
+    return q, sc, zc, steps
+
+
+def dequant_w4c(q, sc, zc, steps) -> np.ndarray:
+    N, K = q.shape
+    out = np.empty((N, K), np.float64)
+    _load().oracle_dequant_w4c(_ptr(q), _ptr(sc), _ptr(zc), _ptr(np.ascontiguousarray(steps)),
+                               N, K, _ptr(out))
+    return out
+
+
+def packed_bytes_c(N: int, K: int) -> int:
+    return int(_load().oracle_packed_bytes_c(N, K))
+
+
+def pack_w4c(q, sc, zc, steps) -> np.ndarray:
+    N, K = q.shape
+    out = np.empty(packed_bytes_c(N, K), np.uint8)
+    _load().oracle_pack_w4c(_ptr(q), _ptr(sc), _ptr(zc), _ptr(np.ascontiguousarray(steps)),
+                            N, K, _ptr(out))
+    return out
+
+
+def unpack_w4c(packed, N: int, K: int):
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    q = np.empty((N, K), np.uint8)
+    sc = np.empty((N, K // GROUP), np.uint8)
+    zc = np.empty((N, K // GROUP), np.uint8)
+    steps = np.empty((N, 2), np.uint16)
+    _load().oracle_unpack_w4c(_ptr(packed), N, K, _ptr(q), _ptr(sc), _ptr(zc), _ptr(steps))
+    return q, sc, zc, steps
+
+
+def w4a16c(x_bf16, q, sc, zc, steps, n0: int = 0, n1: int | None = None) -> np.ndarray:
+    """fp64 out[M, n1-n0] of x . dequant_c(W)[n0:n1]^T."""
+    N, K = q.shape
+    x = _u16(x_bf16).reshape(-1, K)
+    M = x.shape[0]
+    n1 = N if n1 is None else n1
+    out = np.empty((M, n1 - n0), np.float64)
+    _load().oracle_w4a16c(_ptr(x), _ptr(q), _ptr(sc), _ptr(zc), _ptr(np.ascontiguousarray(steps)),
+                          M, N, K, n0, n1, _ptr(out))
+    return out

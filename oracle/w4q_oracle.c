@@ -299,6 +299,257 @@ void oracle_w4a16(const uint16_t *x, const uint8_t *q, const uint16_t *s,
 }
 
 /* ------------------------------------------------------------------ */
+/* Compact metadata: uint8 scale / zero codes on per-row fp16 steps     */
+/* ([T] CudaCoalescedInt4Tensor: scale and zero_point uint8 [N, K/32],  */
+/* scale_step and zero_point_step float16 [N, 1]; the page prints no    */
+/* dequant formula, so this is the reading taken: code x step for both) */
+/* ------------------------------------------------------------------ */
+
+/* fp16 bits -> double (exact). */
+static double fp16_to_double(uint16_t h)
+{
+    int e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m + 1024), e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
+/* Smallest fp16 >= v, for finite v >= 0 (+inf bits past 65504).  An fp16
+ * number in [2^e, 2^(e+1)) is a multiple of 2^(e-10); below 2^-14 the
+ * subnormals are multiples of 2^-24. */
+static uint16_t fp16_round_up(double v)
+{
+    if (v <= 0.0)
+        return 0;
+    int e;
+    (void)frexp(v, &e); /* v in [2^(e-1), 2^e) */
+    int lsb = (e - 1) - 10;
+    if (lsb < -24)
+        lsb = -24;
+    double m = ceil(ldexp(v, -lsb)); /* whole multiples of 2^lsb */
+    double r = ldexp(m, lsb);
+    if (r > 65504.0)
+        return 0x7C00;
+    if (r < ldexp(1.0, -14))
+        return (uint16_t)m; /* subnormal: the mantissa field is m */
+    int re;
+    double f = frexp(r, &re); /* r = f * 2^re, f in [0.5, 1) */
+    uint16_t mant = (uint16_t)(ldexp(f, 11) - 1024.0);
+    return (uint16_t)(((re - 1 + 15) << 10) | mant);
+}
+
+/* One row n of W (bf16 [K]) in the compact format:
+ *   per group g: mn, mx; s*_g = (mx - mn) / 15 (a constant group c:
+ *   |c| / 15, or 1 for c = 0);
+ *   scale step ds = RU_fp16(max_g s*_g / 255); scale code
+ *   sc_g = min(255, ceil(s*_g / ds)); scale s_g = sc_g * ds (>= s*_g);
+ *   z*_g = clamp(-mn / s_g, 0, 15); zero step dz = RU_fp16(max_g z*_g / 255)
+ *   (1 when every z*_g is 0); zero code zc_g = min(255, rint(z*_g / dz));
+ *   zero z_g = zc_g * dz;
+ *   q = clamp(rint(w / s_g + z_g), 0, 15)  (fp64, in this order);
+ *   dequant(q) = (q - z_g) * s_g.
+ * steps[2n] = ds, steps[2n + 1] = dz (fp16 bits). */
+static void quantize_row_c(const uint16_t *w, int64_t K, uint8_t *q, uint8_t *sc,
+                           uint8_t *zc, uint16_t *steps)
+{
+    int64_t G = K / GROUP;
+    double smax = 0.0;
+    for (int64_t g = 0; g < G; ++g) {
+        double mx = -INFINITY, mn = INFINITY;
+        for (int i = 0; i < GROUP; ++i) {
+            double v = bf16_to_double(w[g * GROUP + i]);
+            if (v > mx) mx = v;
+            if (v < mn) mn = v;
+        }
+        double st = (mx == mn) ? (mx == 0.0 ? 1.0 : fabs(mx) / 15.0) : (mx - mn) / 15.0;
+        if (st > smax)
+            smax = st;
+    }
+    uint16_t dsb = fp16_round_up(smax / 255.0);
+    double ds = fp16_to_double(dsb);
+    double zmax = 0.0;
+    for (int64_t g = 0; g < G; ++g) {
+        double mx = -INFINITY, mn = INFINITY;
+        for (int i = 0; i < GROUP; ++i) {
+            double v = bf16_to_double(w[g * GROUP + i]);
+            if (v > mx) mx = v;
+            if (v < mn) mn = v;
+        }
+        double st = (mx == mn) ? (mx == 0.0 ? 1.0 : fabs(mx) / 15.0) : (mx - mn) / 15.0;
+        double c = ceil(st / ds);
+        if (c > 255.0) c = 255.0;
+        if (c < 1.0) c = 1.0;
+        sc[g] = (uint8_t)c;
+        double zs = clamp_code(-mn / ((double)sc[g] * ds));
+        if (zs > zmax)
+            zmax = zs;
+    }
+    uint16_t dzb = zmax > 0.0 ? fp16_round_up(zmax / 255.0) : (uint16_t)0x3C00; /* 1.0 */
+    double dz = fp16_to_double(dzb);
+    for (int64_t g = 0; g < G; ++g) {
+        double mn = INFINITY;
+        for (int i = 0; i < GROUP; ++i) {
+            double v = bf16_to_double(w[g * GROUP + i]);
+            if (v < mn) mn = v;
+        }
+        double s = (double)sc[g] * ds;
+        double zs = clamp_code(-mn / s);
+        double c = rint(zs / dz);
+        if (c > 255.0) c = 255.0;
+        zc[g] = (uint8_t)c;
+        double z = (double)zc[g] * dz;
+        for (int i = 0; i < GROUP; ++i) {
+            double t = bf16_to_double(w[g * GROUP + i]) / s;
+            q[g * GROUP + i] = (uint8_t)clamp_code(rint(t + z));
+        }
+    }
+    steps[0] = dsb;
+    steps[1] = dzb;
+}
+
+/* W bf16 [N,K] -> q u8 [N,K], sc u8 [N,K/32], zc u8 [N,K/32], steps fp16 [N][2]. */
+void oracle_quantize_w4c(const uint16_t *W, int64_t N, int64_t K, uint8_t *q, uint8_t *sc,
+                         uint8_t *zc, uint16_t *steps)
+{
+    int64_t G = K / GROUP;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        quantize_row_c(W + n * K, K, q + n * K, sc + n * G, zc + n * G, steps + 2 * n);
+}
+
+/* dequant(q)[n,k] = (q - zc * dz_n) * (sc * ds_n), exact in fp64. */
+void oracle_dequant_w4c(const uint8_t *q, const uint8_t *sc, const uint8_t *zc,
+                        const uint16_t *steps, int64_t N, int64_t K, double *What)
+{
+    int64_t G = K / GROUP;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        double ds = fp16_to_double(steps[2 * n]), dz = fp16_to_double(steps[2 * n + 1]);
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t g = k / GROUP;
+            double s = (double)sc[n * G + g] * ds, z = (double)zc[n * G + g] * dz;
+            What[n * K + k] = ((double)q[n * K + k] - z) * s;
+        }
+    }
+}
+
+/* Compact packed layout (this library's own): tiles of 16 rows x 256 K as
+ * in the standard layout but 2304 bytes, [2048 B codes][128 B scale codes]
+ * [128 B zero codes], the code pair (row r, row r + 8) of group g at
+ * 2048 + 16 r + 2 g (scales) and 2176 + 16 r + 2 g (zeros); after all
+ * tiles, the fp16 steps (ds, dz) of every row (N padded to 128, padding
+ * zero). */
+#define CTILE_BYTES 2304
+
+int64_t oracle_packed_bytes_c(int64_t N, int64_t K)
+{
+    if (N < 1 || K < TILE_K || K % TILE_K != 0)
+        return 0;
+    int64_t groups = (N + TILE_ROWS * GROUP_TILES - 1) / (TILE_ROWS * GROUP_TILES);
+    return groups * GROUP_TILES * (K / TILE_K) * CTILE_BYTES + groups * 128 * 4;
+}
+
+static int64_t ctile_offset(int64_t t, int64_t b, int64_t KB)
+{
+    int64_t g = t / GROUP_TILES, w = t % GROUP_TILES;
+    return ((g * KB + b) * GROUP_TILES + w) * CTILE_BYTES;
+}
+
+/* The same nibble placement inside a tile as the standard layout. */
+static void cnibble_position(int64_t n, int64_t k, int64_t KB, int64_t *byte, int *shift)
+{
+    int64_t t = n / TILE_ROWS, b = k / TILE_K;
+    int rr = (int)(n % TILE_ROWS), kk = (int)(k % TILE_K);
+    int sb = kk / 64, j = (kk % 64) / 16, col = kk % 16;
+    int rlo = rr % 8, a = rr / 8;
+    int e = col / 8, cc = col % 8;
+    int h = cc % 2, c = cc - h;
+    int l = rlo * 4 + c / 2;
+    int bit = 8 * a + 4 * e + 16 * h;
+    *byte = ctile_offset(t, b, KB) + 512 * sb + 16 * l + 4 * j + bit / 8;
+    *shift = bit % 8;
+}
+
+void oracle_pack_w4c(const uint8_t *q, const uint8_t *sc, const uint8_t *zc,
+                     const uint16_t *steps, int64_t N, int64_t K, uint8_t *packed)
+{
+    int64_t KB = K / TILE_K, G = K / GROUP;
+    int64_t total = oracle_packed_bytes_c(N, K);
+    int64_t tiles = total - ((N + 127) / 128) * 128 * 4;
+    memset(packed, 0, (size_t)total);
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t byte;
+            int shift;
+            cnibble_position(n, k, KB, &byte, &shift);
+            packed[byte] |= (uint8_t)((q[n * K + k] & 0xF) << shift);
+        }
+        int64_t t = n / TILE_ROWS;
+        int rr = (int)(n % TILE_ROWS), r = rr % 8, half = rr / 8;
+        for (int64_t g = 0; g < G; ++g) {
+            int64_t base = ctile_offset(t, g / 8, KB);
+            int gg = (int)(g % 8);
+            packed[base + 2048 + 16 * r + 2 * gg + half] = sc[n * G + g];
+            packed[base + 2176 + 16 * r + 2 * gg + half] = zc[n * G + g];
+        }
+        memcpy(packed + tiles + 4 * n, steps + 2 * n, 4);
+    }
+}
+
+void oracle_unpack_w4c(const uint8_t *packed, int64_t N, int64_t K, uint8_t *q, uint8_t *sc,
+                       uint8_t *zc, uint16_t *steps)
+{
+    int64_t KB = K / TILE_K, G = K / GROUP;
+    int64_t tiles = oracle_packed_bytes_c(N, K) - ((N + 127) / 128) * 128 * 4;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t byte;
+            int shift;
+            cnibble_position(n, k, KB, &byte, &shift);
+            q[n * K + k] = (uint8_t)((packed[byte] >> shift) & 0xF);
+        }
+        int64_t t = n / TILE_ROWS;
+        int rr = (int)(n % TILE_ROWS), r = rr % 8, half = rr / 8;
+        for (int64_t g = 0; g < G; ++g) {
+            int64_t base = ctile_offset(t, g / 8, KB);
+            int gg = (int)(g % 8);
+            sc[n * G + g] = packed[base + 2048 + 16 * r + 2 * gg + half];
+            zc[n * G + g] = packed[base + 2176 + 16 * r + 2 * gg + half];
+        }
+        memcpy(steps + 2 * n, packed + tiles + 4 * n, 4);
+    }
+}
+
+/* out[m, n - n0] = sum_k x[m,k] * (q - zc dz) * (sc ds) in fp64. */
+void oracle_w4a16c(const uint16_t *x, const uint8_t *q, const uint8_t *sc, const uint8_t *zc,
+                   const uint16_t *steps, int64_t M, int64_t N, int64_t K, int64_t n0,
+                   int64_t n1, double *out)
+{
+    (void)N;
+    int64_t G = K / GROUP, W = n1 - n0;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = n0; n < n1; ++n) {
+        double ds = fp16_to_double(steps[2 * n]), dz = fp16_to_double(steps[2 * n + 1]);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t g = k / GROUP;
+                double wq = ((double)q[n * K + k] - (double)zc[n * G + g] * dz) *
+                            ((double)sc[n * G + g] * ds);
+                acc += bf16_to_double(x[m * K + k]) * wq;
+            }
+            out[m * W + (n - n0)] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* W4A8: symmetric int8 activations, one scale per (row, group of 32)   */
 /* ([T] W4A8 bucket kernels, Int4QuantizedGemmPrecisionTest)            */
 /* ------------------------------------------------------------------ */

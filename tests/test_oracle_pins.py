@@ -604,3 +604,217 @@ def test_w8_matches_library_matmul():
     W, scales, x = workloads.w8_inputs(N=128, K=1024, M=3, seed=92)
     ref = (x.double() @ W.double().T * scales.double()).numpy()
     np.testing.assert_allclose(oracle.w8(x, W.numpy(), scales), ref, rtol=1e-12, atol=1e-9)
+
+
+# --------------------------------------------------------------------------
+# Compact metadata: uint8 scale / zero codes on per-row fp16 steps
+# ("test_int4_quantized_gemm.py", CudaCoalescedInt4Tensor: scale and
+# zero_point uint8 [N, K/32], scale_step and zero_point_step float16 [N, 1];
+# read as code x step for both)
+# --------------------------------------------------------------------------
+
+_FP16 = None
+
+
+def positive_fp16():
+    """Every finite positive fp16 as (value, bits), sorted (by enumeration)."""
+    global _FP16
+    if _FP16 is None:
+        bits = np.arange(1, 0x7C00, dtype=np.uint16)
+        vals = bits.view(np.float16).astype(np.float64)
+        _FP16 = (vals, bits)
+    return _FP16
+
+
+def ru_fp16_search(v):
+    """Smallest fp16 >= v > 0, by search over every fp16 number."""
+    vals, bits = positive_fp16()
+    i = int(np.searchsorted(vals, v, side="left"))
+    return float(vals[i]), int(bits[i])
+
+
+def brute_quant_row_c(wbits):
+    """A restatement of the compact quantizer on one row, from its definition:
+    IEEE fp64 steps (Python floats), fp16 rounding up by search, round half
+    to even."""
+    vals = [bits_to_float(b) for b in wbits]
+    G = len(vals) // GROUP
+    groups = [vals[GROUP * g:GROUP * (g + 1)] for g in range(G)]
+
+    def sstar(gv):
+        mx, mn = max(gv), min(gv)
+        if mx == mn:
+            return 1.0 if mx == 0 else abs(mx) / 15.0
+        return (mx - mn) / 15.0
+    ds, dsb = ru_fp16_search(max(sstar(gv) for gv in groups) / 255.0)
+    sc = [min(255, max(1, int(np.ceil(sstar(gv) / ds)))) for gv in groups]
+    zs = [min(15.0, max(0.0, -min(gv) / (c * ds))) for gv, c in zip(groups, sc)]
+    if max(zs) > 0:
+        dz, dzb = ru_fp16_search(max(zs) / 255.0)
+    else:
+        dz, dzb = 1.0, 0x3C00
+    zc = [min(255, round(z / dz)) for z in zs]
+    q = []
+    for gv, c, zz in zip(groups, sc, zc):
+        s, z = c * ds, zz * dz
+        q += [min(15, max(0, round(v / s + z))) for v in gv]
+    return q, sc, zc, (dsb, dzb)
+
+
+@pytest.mark.parametrize("name", ["randn", "scaled", "constant", "zeros", "same_sign", "tiny", "big"])
+def test_compact_quantizer_matches_restatement(name):
+    K = 256
+    rng = np.random.default_rng(170 + len(name))
+    v = rng.standard_normal((4, K))
+    if name == "scaled":
+        v *= 2.0 ** rng.integers(-6, 7, (4, K // GROUP)).repeat(GROUP, axis=1)
+    elif name == "constant":
+        v[:, :GROUP] = 3.0
+        v[:, GROUP:2 * GROUP] = -0.5
+    elif name == "zeros":
+        v[:, :3 * GROUP] = 0.0
+    elif name == "same_sign":
+        v[:, :GROUP] = np.abs(v[:, :GROUP]) + 1.0
+        v[:, GROUP:2 * GROUP] = -np.abs(v[:, GROUP:2 * GROUP]) - 2.0
+    elif name == "tiny":
+        v *= 1e-3
+    elif name == "big":
+        v *= 300.0
+    W = torch.tensor(v, dtype=torch.float32).to(torch.bfloat16)
+    wb = W.view(torch.int16).numpy().view(np.uint16)
+    q, sc, zc, st = oracle.quantize_w4c(W, 4, K)
+    for n in range(4):
+        bq, bsc, bzc, bst = brute_quant_row_c(wb[n])
+        assert list(q[n]) == bq, (name, n)
+        assert list(sc[n]) == bsc and list(zc[n]) == bzc, (name, n)
+        assert tuple(int(x) for x in st[n]) == bst, (name, n)
+
+
+def test_compact_quantizer_hand_derived_row():
+    # one row, two groups: group 0 spans [-1, 2] (s* = 0.2), group 1 spans
+    # [-0.5, 1] (s* = 0.1); ds = RU_fp16(0.2 / 255): 0.2/255 = 7.84e-4 lies
+    # in [2^-11, 2^-10), fp16 spacing 2^-21 there, so ds = 1645 * 2^-21;
+    # sc = ceil(s* / ds) = 255 and 128
+    K = 64
+    g0 = [-1.0, 2.0] + [0.5] * 30
+    g1 = [-0.5, 1.0] + [0.25] * 30
+    x = np.array([[float_to_bits(v) for v in g0 + g1]], np.uint16)
+    q, sc, zc, st = oracle.quantize_w4c(x, 1, K)
+    ds = float(np.array([st[0, 0]], np.uint16).view(np.float16)[0])
+    assert ds == 1645 * 2.0 ** -21
+    assert list(sc[0]) == [255, 128]
+    s0, s1 = 255 * ds, 128 * ds
+    assert s0 >= 0.2 and s1 >= 0.1
+    # the codes of the ends of each group land on 0 and 15 or next to them
+    assert q[0, 0] == 0 and q[0, 32] == 0
+    assert q[0, 1] == 15 and q[0, 33] == 15
+
+
+def test_compact_quantizer_invariants_on_randn():
+    N, K = 256, 1024
+    W = workloads.w4_weight(N, K, seed=171)
+    q, sc, zc, st = oracle.quantize_w4c(W, N, K)
+    assert q.max() <= 15 and sc.min() >= 1
+    wh = oracle.dequant_w4c(q, sc, zc, st)
+    w = W.double().numpy()
+    ds = st[:, 0].view(np.float16).astype(np.float64)
+    s = sc.astype(np.float64) * ds[:, None]                       # [N, G]
+    g = w.reshape(N, K // GROUP, GROUP)
+    sstar = (g.max(axis=2) - g.min(axis=2)) / 15.0
+    assert (s >= sstar).all()                                     # the scale code rounds up
+    vals, _ = positive_fp16()
+    smax = sstar.max(axis=1) / 255.0
+    assert (ds >= smax).all()
+    below = vals[np.searchsorted(vals, ds) - 1]                   # the next smaller fp16
+    assert (below < smax).all()                                   # ds is the least such
+    straddle = (g.min(axis=2) <= 0) & (g.max(axis=2) >= 0)
+    err = np.abs(w - wh).reshape(N, K // GROUP, GROUP).max(axis=2)
+    assert (err[straddle] <= s[straddle] / 2 * (1 + 1e-12)).all()
+
+
+def test_compact_zero_group_dequantizes_to_zero():
+    K = 64
+    x = np.zeros((1, K), np.uint16)
+    x[0, 32:] = [float_to_bits(v / 16.0) for v in range(-16, 16)]
+    q, sc, zc, st = oracle.quantize_w4c(x, 1, K)
+    assert (oracle.dequant_w4c(q, sc, zc, st)[0, :32] == 0).all()
+
+
+def decode_layout_c(packed, N, K):
+    """Independent decoder of the compact layout (nibbles as the standard
+    layout, 2304-byte tiles, code pairs, steps after the tiles)."""
+    KB, G = K // 256, K // GROUP
+    Np = (N + 127) // 128 * 128
+    tiles = packed[: (Np // 128) * 8 * KB * 2304].reshape(Np // 128, KB, 8, 2304)
+    q = np.zeros((Np, K), np.uint8)
+    sc = np.zeros((Np, G), np.uint8)
+    zc = np.zeros((Np, G), np.uint8)
+    for gp in range(Np // 128):
+        for b in range(KB):
+            for t in range(8):
+                tile = tiles[gp, b, t]
+                rows = gp * 128 + t * 16
+                codes = tile[:2048].reshape(4, 32, 4, 4)      # [sub-block][lane][word][byte]
+                words = codes.copy().view(np.uint32).reshape(4, 32, 4)
+                for l in range(32):
+                    r, c = l // 4, 2 * (l % 4)
+                    for sbk in range(4):
+                        for j in range(4):
+                            w = int(words[sbk, l, j])
+                            for a in range(2):
+                                for e in range(2):
+                                    for h in range(2):
+                                        q[rows + r + 8 * a, 256 * b + 64 * sbk + 16 * j + c + 8 * e + h] = \
+                                            (w >> (8 * a + 4 * e + 16 * h)) & 0xF
+                for r in range(8):
+                    for gg in range(8):
+                        for half in range(2):
+                            sc[rows + r + 8 * half, 8 * b + gg] = tile[2048 + 16 * r + 2 * gg + half]
+                            zc[rows + r + 8 * half, 8 * b + gg] = tile[2176 + 16 * r + 2 * gg + half]
+    steps = packed[(Np // 128) * 8 * KB * 2304:].view(np.uint16).reshape(Np, 2)
+    return q[:N], sc[:N], zc[:N], steps[:N]
+
+
+@pytest.mark.parametrize("N,K", [(16, 256), (130, 512)])
+def test_compact_pack_matches_independent_decoder(N, K):
+    W = workloads.w4_weight(N, K, seed=172)
+    q, sc, zc, st = oracle.quantize_w4c(W, N, K)
+    packed = oracle.pack_w4c(q, sc, zc, st)
+    assert packed.size == oracle.packed_bytes_c(N, K) == \
+        (N + 127) // 128 * (8 * (K // 256) * 2304 + 128 * 4)
+    dq, dsc, dzc, dst = decode_layout_c(packed, N, K)
+    assert np.array_equal(dq, q) and np.array_equal(dsc, sc) and np.array_equal(dzc, zc)
+    assert np.array_equal(dst, st)
+    uq, usc, uzc, ust = oracle.unpack_w4c(packed, N, K)
+    assert np.array_equal(uq, q) and np.array_equal(usc, sc) and np.array_equal(ust, st)
+
+
+def test_compact_pack_hand_derived_positions():
+    # row 9 = tile 0 row r = 1 of its upper half, group 3 of super-block 0:
+    # scale code at 2048 + 16 * 1 + 2 * 3 + 1 = 2071, zero code at 2199;
+    # row 130 (tile group 1, tile 0, row 2), K = 512: its steps at
+    # 2 * 8 * 2 * 2304 + 4 * 130
+    N, K = 140, 512
+    q = np.zeros((N, K), np.uint8)
+    sc = np.ones((N, K // GROUP), np.uint8)
+    zc = np.zeros((N, K // GROUP), np.uint8)
+    st = np.zeros((N, 2), np.uint16)
+    sc[9, 3], zc[9, 3] = 77, 99
+    st[130] = (0x1234, 0x5678)
+    p = oracle.pack_w4c(q, sc, zc, st)
+    assert p[2071] == 77 and p[2199] == 99
+    off = 2 * 8 * 2 * 2304 + 4 * 130
+    assert p[off:off + 4].tobytes() == bytes([0x34, 0x12, 0x78, 0x56])
+
+
+def test_compact_w4a16_matches_library_matmul_and_one_hot():
+    N, K, M = 96, 512, 3
+    W = workloads.w4_weight(N, K, seed=173)
+    q, sc, zc, st = oracle.quantize_w4c(W, N, K)
+    wh = oracle.dequant_w4c(q, sc, zc, st)
+    x = torch.randn(M, K, generator=torch.Generator().manual_seed(174)).to(torch.bfloat16)
+    ref = x.double().numpy() @ wh.T
+    np.testing.assert_allclose(oracle.w4a16c(x, q, sc, zc, st), ref, rtol=1e-12, atol=1e-12)
+    e = torch.zeros(1, K, dtype=torch.bfloat16)
+    e[0, 77] = 1.0
+    np.testing.assert_array_equal(oracle.w4a16c(e, q, sc, zc, st)[0], wh[:, 77])
