@@ -79,7 +79,8 @@ PAGES_W8_GBS = 1277.19   # "gpt-fast issue #114": compiled int8 GEMV, 8192^2, M=
 
 def step_calls():
     """(kind, N, K, M) of one step, in launch order.  Kinds: w8, w4a16, w4a8r
-    (W4A8, one activation scale per row), w4a8 (one per group of 32)."""
+    (W4A8, one activation scale per row), w4a8 (one per group of 32), w4a16c
+    (W4A16 with the compact metadata)."""
     calls = [("w8", workloads.W8_GEMV["N"], workloads.W8_GEMV["K"], 1),
              ("w4a16", workloads.TINY_W4A16["N"], workloads.TINY_W4A16["K"], 1)]
     for (N, K) in workloads.W4A16_GEMV_SHAPES:
@@ -89,6 +90,9 @@ def step_calls():
     for kind in ("w4a8r", "w4a8"):
         for M in workloads.W4A8_MS:
             calls.append((kind, N, K, M))
+    # the compact metadata (uint8 scale / zero codes on fp16 row steps)
+    for (N, K) in ((6656, 19968), (8448, 6656)):
+        calls.append(("w4a16c", N, K, 1))
     for (N, K) in workloads.TC_SHAPES:
         for M in workloads.TC_MS:
             calls.append(("w4a16", N, K, M))
@@ -99,6 +103,8 @@ def weight_bytes(kind, N, K):
     """Bytes of weights + scales + zeros the call must read (the metric)."""
     if kind == "w8":
         return N * K + 2 * N
+    if kind == "w4a16c":
+        return N * K // 2 + 2 * N * K // 32 + 4 * N
     return N * K // 2 + 3 * N * K // 32
 
 
@@ -118,6 +124,8 @@ def kernel_name(kind, M, launches=None):
         return "w8_kernel<M=%d>" % M
     if kind == "w4a16" and M >= 9:
         return "w4_umma_kernel<NP=%d>" % ((M + 15) // 16 * 16)
+    if kind == "w4a16c":
+        return "w4_cluster_kernel<A16,compact>"
     mode = "A16" if kind == "w4a16" else "A8"
     if launches == 1:
         return "w4_cluster_kernel<%s>" % mode
@@ -211,7 +219,7 @@ class Suite:
             users[key] = users.get(key, 0) + 1
         for key, n_users in users.items():
             kind, N, K = key
-            per = weight_bytes(kind, N, K)
+            per = weight_bytes("w4a16c" if kind == "w4c" else kind, N, K)
             copies = max(n_users + 1, -(-3 * l2_bytes // per), 4)
             if kind == "w8":
                 W, sc, _ = workloads.w8_inputs(N=N, K=K, M=1)
@@ -219,7 +227,7 @@ class Suite:
                 self.extra[key] = sc.to(dev)
             else:
                 W = workloads.w4_weight(N, K).to(dev)
-                base = w4q.w4_pack_weights(W)
+                base = w4q.w4_pack_weights_compact(W) if kind == "w4c" else w4q.w4_pack_weights(W)
                 del W
             pool = [base] + [base.clone() for _ in range(copies - 1)]
             self.pools[key] = pool
@@ -229,15 +237,16 @@ class Suite:
             self.x[i] = x.to(dev)
             self.out[i] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             self.out_host[i] = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
-            if kind != "w8":
+            if kind not in ("w8", "w4a16c"):
                 nbytes = max(w4q.workspace_bytes(M, N, K), 16)
                 self.ws[i] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
     @staticmethod
     def wkey(kind, N, K):
-        """The weight pool a call reads (every W4 kind shares the packed format)."""
-        return ("w8" if kind == "w8" else "w4", N, K)
+        """The weight pool a call reads (the W4 kinds share the packed format,
+        except the compact one)."""
+        return ("w8" if kind == "w8" else ("w4c" if kind == "w4a16c" else "w4"), N, K)
 
     def launch(self, i, copy_index, x=None, out=None):
         kind, N, K, M = self.calls[i]
@@ -251,13 +260,15 @@ class Suite:
             self.w4q.w4a16_gemm(x, w, N, K, out=out, workspace=self.ws[i])
         elif kind == "w4a8r":
             self.w4q.w4a8_gemm_rowscale(x, w, N, K, out=out, workspace=self.ws[i])
+        elif kind == "w4a16c":
+            self.w4q.w4a16_gemm_compact(x, w, N, K, out=out)
         else:
             self.w4q.w4a8_gemm(x, w, N, K, out=out, workspace=self.ws[i])
 
     def launches_per_step(self):
         n = 0
         for kind, N, K, M in self.calls:
-            n += 1 if kind == "w8" else self.w4q.kernel_launches(
+            n += 1 if kind in ("w8", "w4a16c") else self.w4q.kernel_launches(
                 M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
         return n
 
@@ -301,7 +312,7 @@ def measure_calls(suite, reps=3):
             b.synchronize()
             times.append(a.elapsed_time(b) * 1e3 / R)
         us = statistics.median(times[1:])
-        launches = None if kind == "w8" else suite.w4q.kernel_launches(
+        launches = None if kind in ("w8", "w4a16c") else suite.w4q.kernel_launches(
             M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
         res.append(dict(call=call_label(kind, N, K, M), kind=kind, N=N, K=K, M=M,
                         kernel=kernel_name(kind, M, launches), us=us,
@@ -548,6 +559,9 @@ def _oracle_sample(frac_rows):
             Wr = W[:rows].numpy().copy()
             scr = sc[:rows].clone()
             jobs.append(("w8", x, (Wr, scr), rows, K))
+        elif kind == "w4a16c":
+            Wd = workloads.w4_weight(N, K)[:rows].contiguous()
+            jobs.append((kind, x, oracle.pack_w4c(*oracle.quantize_w4c(Wd, rows, K)), rows, K))
         else:
             key = (N, K)
             if key not in cache:
@@ -563,6 +577,9 @@ def _oracle_sample(frac_rows):
         for kind, x, data, rows, K in jobs:
             if kind == "w8":
                 oracle.w8(x, data[0], data[1])
+                continue
+            if kind == "w4a16c":
+                oracle.w4a16c(x, *oracle.unpack_w4c(data, rows, K))
                 continue
             q, s, z = oracle.unpack_w4(data, rows, K)
             if kind == "w4a16":
@@ -654,11 +671,15 @@ def profile_call(spec, launches):
         W, sc = W.to(dev), sc.to(dev)
         fn = lambda: w4q.w8_gemv(x, W, sc)  # noqa: E731
     else:
-        packed = w4q.w4_pack_weights(workloads.w4_weight(N, K).to(dev))
-        op = {"w4a16": w4q.w4a16_gemm, "w4a8": w4q.w4a8_gemm,
-              "w4a8r": w4q.w4a8_gemm_rowscale}[kind]
-        ws = torch.empty(max(w4q.workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
-        fn = lambda: op(x, packed, N, K, workspace=ws)  # noqa: E731
+        if kind == "w4a16c":
+            packed = w4q.w4_pack_weights_compact(workloads.w4_weight(N, K).to(dev))
+            fn = lambda: w4q.w4a16_gemm_compact(x, packed, N, K)  # noqa: E731
+        else:
+            packed = w4q.w4_pack_weights(workloads.w4_weight(N, K).to(dev))
+            op = {"w4a16": w4q.w4a16_gemm, "w4a8": w4q.w4a8_gemm,
+                  "w4a8r": w4q.w4a8_gemm_rowscale}[kind]
+            ws = torch.empty(max(w4q.workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
+            fn = lambda: op(x, packed, N, K, workspace=ws)  # noqa: E731
     for _ in range(2 + launches):
         fn()
     torch.cuda.synchronize()

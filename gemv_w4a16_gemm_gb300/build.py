@@ -14,8 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libw4q.so")
-SOURCES = ("api.cu", "pack.cu", "gemv_w4.cu", "gemv_w4_cluster.cu", "gemv_w4_umma.cu", "w8.cu",
-           "noalloc.cu", "selftest.cu")
+SOURCES = ("api.cu", "pack.cu", "pack_compact.cu", "gemv_w4.cu", "gemv_w4_cluster.cu",
+           "gemv_w4_umma.cu", "w8.cu", "noalloc.cu", "selftest.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -70,7 +70,8 @@ int check_w4_shape(int64_t M, int64_t N, int64_t K, int group)
 
 int gemm_common(w4q::W4Mode mode, const void *x, const void *packed, void *out, int64_t M,
                 int64_t N, int64_t K, int group, int split, void *workspace,
-                size_t workspace_bytes, int32_t *dots, void *stream, bool act_row = false)
+                size_t workspace_bytes, int32_t *dots, void *stream, bool act_row = false,
+                bool compact = false)
 {
     if (x == nullptr || packed == nullptr || (out == nullptr && dots == nullptr))
         return W4Q_ERR_INVALID_ARG;
@@ -88,7 +89,8 @@ int gemm_common(w4q::W4Mode mode, const void *x, const void *packed, void *out, 
     if (dev < 0)
         return W4Q_ERR_CUDA;
     w4q::W4Plan plan;
-    if (!w4q::w4_plan((int)M, (int)N, (int)K, split, sm_count(dev), mode, &plan, act_row))
+    if (!w4q::w4_plan((int)M, (int)N, (int)K, split, sm_count(dev), mode, &plan, act_row,
+                      compact))
         return W4Q_ERR_UNSUPPORTED;
     const size_t need = w4q::w4_workspace_for(plan, mode);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need))
@@ -326,6 +328,55 @@ int w4a8_gemm_rowscale_split(const void *x_bf16, const void *packed, void *out_b
         return W4Q_ERR_INVALID_ARG;
     return gemm_common(w4q::W4Mode::A8, x_bf16, packed, out_bf16, M, N, K, group, split_k,
                        workspace, workspace_bytes, nullptr, stream, true);
+}
+
+size_t w4_packed_bytes_compact(int64_t N, int64_t K, int group)
+{
+    if (check_w4_shape(1, N, K, group) != W4Q_OK)
+        return 0;
+    return w4q::packed_bytes_compact((int)N, (int)K);
+}
+
+int w4_pack_weights_compact(const void *W_bf16, int64_t N, int64_t K, int group, void *packed,
+                            void *stream)
+{
+    if (W_bf16 == nullptr || packed == nullptr)
+        return W4Q_ERR_INVALID_ARG;
+    int st = check_w4_shape(1, N, K, group);
+    if (st != W4Q_OK)
+        return st;
+    if (!aligned16(W_bf16) || !aligned16(packed))
+        return W4Q_ERR_MISALIGNED;
+    cudaError_t e = w4q::launch_pack_compact(W_bf16, packed, (int)N, (int)K,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
+}
+
+int w4_unpack_weights_compact(const void *packed, int64_t N, int64_t K, int group, uint8_t *q,
+                              uint8_t *scale_codes, uint8_t *zero_codes, void *steps_fp16,
+                              void *stream)
+{
+    if (packed == nullptr || q == nullptr || scale_codes == nullptr || zero_codes == nullptr ||
+        steps_fp16 == nullptr)
+        return W4Q_ERR_INVALID_ARG;
+    int st = check_w4_shape(1, N, K, group);
+    if (st != W4Q_OK)
+        return st;
+    if (!aligned16(packed) || !aligned16(q) || !aligned16(scale_codes) || !aligned16(zero_codes) ||
+        !aligned16(steps_fp16))
+        return W4Q_ERR_MISALIGNED;
+    cudaError_t e = w4q::launch_unpack_compact(packed, q, scale_codes, zero_codes, steps_fp16,
+                                               (int)N, (int)K, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
+}
+
+int w4a16_gemm_compact(const void *x_bf16, const void *packed, void *out_bf16, int64_t M,
+                       int64_t N, int64_t K, int group, void *stream)
+{
+    if (M > 8)
+        return W4Q_ERR_UNSUPPORTED;
+    return gemm_common(w4q::W4Mode::A16, x_bf16, packed, out_bf16, M, N, K, group, -1, nullptr,
+                       0, nullptr, stream, false, true);
 }
 
 int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16, void *out_bf16,

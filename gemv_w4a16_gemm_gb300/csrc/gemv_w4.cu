@@ -880,7 +880,7 @@ int cluster_choice(int M, int G, int KB, int sm_count)
 }  // namespace
 
 bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan,
-             bool act_row)
+             bool act_row, bool compact)
 {
     if (M < 1 || M > 64 || N < 1 || K < 256 || K % 256 != 0)
         return false;
@@ -907,6 +907,8 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
     // library's own choice and explicit splits of 1..8 whenever the slice
     // of activations it keeps in shared memory fits; stream-K (split 0),
     // larger explicit splits and the longest K stay on the stream-K kernel.
+    if (compact && (pl.umma || mode != W4Mode::A16))
+        return false;  // the compact metadata is read by the cluster kernel (W4A16, M <= 8)
     if (!pl.umma && split < 0) {
         // a measured choice for this call, if the table has one
         const int t = table_split(sm_count, mode == W4Mode::A16 ? 0 : (act_row ? 2 : 1), M, N, K);
@@ -914,11 +916,14 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
             split = t;
     }
     if (!pl.umma) {
-        const int C = split < 0 ? cluster_choice(M, pl.G, pl.KB, sm_count)
-                                : (split >= 1 && split <= 8 && w4_cluster_ring(M, pl.KB, split) > 0
-                                       ? split : 0);
+        int C = split < 0 ? cluster_choice(M, pl.G, pl.KB, sm_count)
+                          : (split >= 1 && split <= 8 && w4_cluster_ring(M, pl.KB, split) > 0
+                                 ? split : 0);
+        if (compact && C == 0 && split <= 0)
+            C = cluster_choice(M, pl.G, pl.KB, sm_count);  // never the stream-K kernel
         if (C > 0) {
             pl.cluster = C;
+            pl.compact = compact;
             pl.split = C;
             pl.P = pl.G * C;
             pl.fixup = false;
@@ -927,6 +932,8 @@ bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *
             return true;
         }
     }
+    if (compact)
+        return false;  // no cluster split fits
     if (mode == W4Mode::A8_DOTS)
         split = 1;  // every unit is processed once; no accumulation across CTAs
     // Tensor-core path with few super-blocks and no more row-group pairs than

@@ -46,6 +46,8 @@
 //    returns.
 #include <atomic>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "timeline.cuh"
@@ -124,12 +126,12 @@ struct CLayout {
 // smax x MP x 32][partial sums: 128 x MP f32][received sums (rank 0):
 // (C-1) x 128 x MP f32][row maxima: own + received, C x 8 u32][16 zero
 // bytes][barriers: 2R ring + received sums + received maxima, x 8]
-__host__ __device__ inline CLayout c_layout(int mp, int smax, int R, int C)
+__host__ __device__ inline CLayout c_layout(int mp, int smax, int R, int C, int tile_bytes)
 {
     CLayout L;
     int o = 0;
     L.ring = o;
-    o += R * WARPS * TILE_BYTES;
+    o += R * WARPS * tile_bytes;
     L.xr = o;
     o += smax * mp * XROW;
     L.xs = o;
@@ -207,16 +209,21 @@ __device__ __forceinline__ void prep_stage_a8(const uint4 (&raw)[MP], int M, int
     }
 }
 
-template <W4Mode MODE, bool ROW, int MP>
+// Tile bytes: the standard metadata (bf16 scale, u8 zero) or the compact one
+// (u8 scale and zero codes; the fp16 row steps after the tiles).
+constexpr int CMP_TILE_BYTES = 2304;
+
+template <W4Mode MODE, bool ROW, int MP, bool CMP>
 __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
 {
     constexpr bool DOTS = MODE == W4Mode::A8_DOTS;
     constexpr bool A16 = MODE == W4Mode::A16;
-    constexpr int SB = WARPS * TILE_BYTES;  // one stage: the 8 tiles of a super-block
+    constexpr int TB = CMP ? CMP_TILE_BYTES : TILE_BYTES;
+    constexpr int SB = WARPS * TB;  // one stage: the 8 tiles of a super-block
     const int R = p.R;
 
     extern __shared__ __align__(128) uint8_t smem[];
-    const CLayout L = c_layout(MP, p.smax, R, p.C);
+    const CLayout L = c_layout(MP, p.smax, R, p.C, TB);
     uint8_t *xr = smem + L.xr, *xs = smem + L.xs, *xg = smem + L.xg;
     float *red = reinterpret_cast<float *>(smem + L.red);
     uint32_t *rowmax = reinterpret_cast<uint32_t *>(smem + L.rowmax);
@@ -389,6 +396,18 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
         }
     } else {
         // ----------------------------------------------------- consumers
+        // compact metadata: this lane's row steps (ds of rows r, r + 8, then
+        // dz), stored after the tiles of the packed buffer
+        float rs[4] = {1.f, 1.f, 1.f, 1.f};
+        if constexpr (CMP) {
+            const int n = (g * WARPS + warp) * 16 + (lane >> 2);
+            const __half *st = reinterpret_cast<const __half *>(
+                p.packed + (size_t)p.G * WARPS * p.KB * CMP_TILE_BYTES);
+            rs[0] = __half2float(st[2 * n]);
+            rs[1] = __half2float(st[2 * (n + 8)]);
+            rs[2] = __half2float(st[2 * n + 1]);
+            rs[3] = __half2float(st[2 * (n + 8) + 1]);
+        }
         for (int i = 0; i < S; ++i) {
             const int slot = i % R;
             const bool got = W4Q_RING_WAIT(full0 + 8 * slot, (uint32_t)(i / R) & 1);
@@ -398,16 +417,16 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
                 break;
             }
             if (tile < p.T) {
-                const uint32_t wbase = smem_addr(smem + L.ring + slot * SB + warp * TILE_BYTES);
+                const uint32_t wbase = smem_addr(smem + L.ring + slot * SB + warp * TB);
                 const uint32_t xb = smem_addr(xr + i * MP * XROW);
                 const uint32_t sb = smem_addr(xs + i * MP * SROW);
                 const uint32_t gb = smem_addr(xg + i * MP * SROW);
                 if constexpr (MP < 8)
-                    compute_stage_packed<MP, DOTS, !A16, A16>(wbase, xb, sb, gb, zrow, lane, acc, p,
-                                                              tile, b0 + i);
+                    compute_stage_packed<MP, DOTS, !A16, A16, CMP>(wbase, xb, sb, gb, zrow, lane,
+                                                                   acc, p, tile, b0 + i, rs);
                 else
-                    compute_stage<1, DOTS, !A16, A16>(wbase, xb, sb, gb, lane, acc, p, tile,
-                                                      b0 + i);
+                    compute_stage<1, DOTS, !A16, A16, CMP>(wbase, xb, sb, gb, lane, acc, p, tile,
+                                                           b0 + i, rs);
             }
             __syncwarp();
             if (lane == 0)
@@ -487,10 +506,10 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
     }
 }
 
-template <W4Mode MODE, bool ROW, int MP>
+template <W4Mode MODE, bool ROW, int MP, bool CMP>
 cudaError_t launch_t(const CParams &p, int smem, cudaStream_t stream)
 {
-    auto fn = w4_cluster_kernel<MODE, ROW, MP>;
+    auto fn = w4_cluster_kernel<MODE, ROW, MP, CMP>;
     // the dynamic shared-memory opt-in, once per device (a bit per device)
     static std::atomic<unsigned long long> opted_in{0};
     int dev = 0;
@@ -521,14 +540,14 @@ cudaError_t launch_t(const CParams &p, int smem, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
-template <W4Mode MODE, bool ROW>
+template <W4Mode MODE, bool ROW, bool CMP = false>
 cudaError_t dispatch_mp(const CParams &p, int mp, int smem, cudaStream_t stream)
 {
     switch (mp) {
-    case 1: return launch_t<MODE, ROW, 1>(p, smem, stream);
-    case 2: return launch_t<MODE, ROW, 2>(p, smem, stream);
-    case 4: return launch_t<MODE, ROW, 4>(p, smem, stream);
-    default: return launch_t<MODE, ROW, 8>(p, smem, stream);
+    case 1: return launch_t<MODE, ROW, 1, CMP>(p, smem, stream);
+    case 2: return launch_t<MODE, ROW, 2, CMP>(p, smem, stream);
+    case 4: return launch_t<MODE, ROW, 4, CMP>(p, smem, stream);
+    default: return launch_t<MODE, ROW, 8, CMP>(p, smem, stream);
     }
 }
 
@@ -545,7 +564,7 @@ int w4_cluster_ring(int M, int KB, int C)
         return 0;
     const int smax = (KB + C - 1) / C;
     for (int R = 4; R >= 2; --R)
-        if (c_layout(mp_of(M), smax, R, C).total <= CTA_SMEM_MAX)
+        if (c_layout(mp_of(M), smax, R, C, TILE_BYTES).total <= CTA_SMEM_MAX)
             return R;
     return 0;
 }
@@ -554,6 +573,7 @@ cudaError_t launch_w4_cluster(const W4Plan &plan, W4Mode mode, bool act_row, con
                               const void *packed, void *out, int32_t *dots, unsigned *err,
                               cudaStream_t stream)
 {
+    const bool cmp = plan.compact;
     CParams p;
     p.packed = static_cast<const uint8_t *>(packed);
     p.x = static_cast<const __nv_bfloat16 *>(x);
@@ -572,7 +592,10 @@ cudaError_t launch_w4_cluster(const W4Plan &plan, W4Mode mode, bool act_row, con
     if (p.R == 0)
         return cudaErrorInvalidValue;
     const int mp = mp_of(plan.M);
-    const int smem = c_layout(mp, p.smax, p.R, p.C).total;
+    const int smem = c_layout(mp, p.smax, p.R, p.C, cmp ? CMP_TILE_BYTES : TILE_BYTES).total;
+    if (cmp)  // compact metadata: W4A16 only
+        return mode == W4Mode::A16 ? dispatch_mp<W4Mode::A16, false, true>(p, mp, smem, stream)
+                                   : cudaErrorInvalidValue;
     if (mode == W4Mode::A16)
         return dispatch_mp<W4Mode::A16, false>(p, mp, smem, stream);
     if (mode == W4Mode::A8)

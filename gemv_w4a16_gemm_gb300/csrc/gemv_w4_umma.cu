@@ -516,11 +516,11 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
     // The fixup launch may start once every CTA is here (it waits for the
     // grid's completion before reading partials); triggering any earlier
     // would park its blocks, waiting, beside the dequant warps.
-    if (threadIdx.x == 0)
-        W4Q_STAMP(42);
     pdl_launch_dependents();
     tc_fence_before_sync();
     __syncthreads();
+    if (threadIdx.x == 0)
+        W4Q_STAMP(42);
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, UT_TMEM_COLS);

@@ -32,15 +32,17 @@ struct W4Plan {
     int NP;         // umma: M rounded up to 16 (the MMA's N)
     int G2;         // umma: ceil(G / 2) pairs of tile groups
     int cluster;    // > 0: the cluster kernel (M <= 8), this many CTAs split each group's K
+    bool compact;   // the packed weight holds the compact metadata (cluster kernel only)
 };
 
 enum class W4Mode { A16, A8, A8_DOTS };
 
 // Plan for these sizes (split: -1 = the library's choice, 0 = stream-K,
 // s >= 1 = fixed).  Returns false when the sizes or split are unsupported.
-// act_row: W4A8 with one activation scale per row (the split table keys it apart).
+// act_row: W4A8 with one activation scale per row (the split table keys it
+// apart).  compact: the compact metadata, which only the cluster kernel reads.
 bool w4_plan(int M, int N, int K, int split, int sm_count, W4Mode mode, W4Plan *plan,
-             bool act_row = false);
+             bool act_row = false, bool compact = false);
 
 // Workspace bytes for a plan (partials + the W4A8 activation buffers).
 size_t w4_workspace_for(const W4Plan &plan, W4Mode mode);
@@ -63,6 +65,12 @@ size_t w4_umma_workspace(const W4Plan &plan);
 size_t w4_umma_partial_bytes(int P, int M);
 cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed, void *out,
                            void *workspace, unsigned *err, cudaStream_t stream);
+
+// --- compact metadata: packer and its inverse view (pack_compact.cu)
+size_t packed_bytes_compact(int N, int K);
+cudaError_t launch_pack_compact(const void *W, void *packed, int N, int K, cudaStream_t stream);
+cudaError_t launch_unpack_compact(const void *packed, uint8_t *q, uint8_t *sc, uint8_t *zc,
+                                  void *steps, int N, int K, cudaStream_t stream);
 
 cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *sx, bool row,
                                 cudaStream_t stream);

@@ -44,22 +44,85 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 
 // The stage functions read only p.M, p.N, p.K and p.dots (the W4A8
 // group-dot export) from the kernel parameters, whichever kernel's they are.
+//
+// CMP: the tile holds the compact metadata (2304-byte tiles: uint8 scale
+// codes at 2048 and zero codes at 2176, the pair of rows r, r + 8 of group
+// g in word g / 2, bytes 2 (g % 2) and 2 (g % 2) + 1); rs holds this lane's
+// row steps (ds of rows r, r + 8, then dz of rows r, r + 8) as fp32.  The
+// scale sc * ds and the zero zc * dz are exact in fp32 (8 x 11 bits).
+
+// bytes [c, 0, 0, 0x4B] = 2^23 + c: the byte c of word w at byte index i
+__device__ __forceinline__ float byte_as_float(uint32_t w, uint32_t i)
+{
+    return __uint_as_float(prmt(w, 0x4B000000u, 0x7440u + i)) - 8388608.0f;
+}
+
+// Group g's scales sr, sr8 and negated zero points nzr, nzr8 of rows r and
+// r + 8, from the standard metadata words (sw: the bf16 pair of the group,
+// zw: the zero bytes' word) or the compact ones (sw: the scale codes' word,
+// zw: the zero codes' word).
+template <bool CMP>
+__device__ __forceinline__ void group_meta(uint32_t sw, uint32_t zw, int g, const float (&rs)[4],
+                                           float &sr, float &sr8, float &nzr, float &nzr8)
+{
+    const uint32_t zb = (uint32_t)((2 * g) & 3);  // byte of row r; row r + 8 follows
+    if constexpr (CMP) {
+        sr = byte_as_float(sw, zb) * rs[0];
+        sr8 = byte_as_float(sw, zb + 1) * rs[1];
+        nzr = -(byte_as_float(zw, zb) * rs[2]);
+        nzr8 = -(byte_as_float(zw, zb + 1) * rs[3]);
+    } else {
+        sr = bf16lo_to_f32(sw);
+        sr8 = bf16hi_to_f32(sw);
+        nzr = -byte_as_float(zw, zb);
+        nzr8 = -byte_as_float(zw, zb + 1);
+    }
+}
+
+// The metadata words of group g for rows r, r + 8, read from the tile.
+template <bool CMP>
+__device__ __forceinline__ void group_meta_words(uint32_t wbase, int r, int g, uint32_t &sw,
+                                                 uint32_t &zw)
+{
+    if constexpr (CMP) {
+        sw = lds32(wbase + 2048 + 16 * r + 4 * (g >> 1));
+        zw = lds32(wbase + 2176 + 16 * r + 4 * (g >> 1));
+    } else {
+        sw = lds32(wbase + 2048 + ((g & 4) ? 128 : 0) + 16 * r + 4 * (g & 3));
+        zw = lds32(wbase + 2304 + 16 * r + 4 * (g >> 1));
+    }
+}
 
 // One stage: this warp's 16 x 256 tile, 4 sub-blocks of 64 K (two groups
 // each), 4 k16 steps per sub-block.  xbase: the stage's activation rows;
 // sbase: the stage's group sums; gbase: per row, the W4A8 group scales (GS)
 // or the stage's row factor c (SC: the stage's sum is scaled once by c).
-template <int NB, bool DOTS, bool GS, bool SC, class PP>
+template <int NB, bool DOTS, bool GS, bool SC, bool CMP = false, class PP>
 __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, uint32_t sbase,
                                               uint32_t gbase, int lane, float (&acc)[NB][4],
-                                              const PP &p, int tile, int b)
+                                              const PP &p, int tile, int b,
+                                              const float (&rs)[4] = {1.f, 1.f, 1.f, 1.f})
 {
     const int r = lane >> 2, c2 = 2 * (lane & 3);
-    const uint4 sc0 = lds128(wbase + 2048 + 16 * r);
-    const uint4 sc1 = lds128(wbase + 2048 + 128 + 16 * r);
-    const uint4 zz = lds128(wbase + 2304 + 16 * r);
-    const uint32_t scw[8] = {sc0.x, sc0.y, sc0.z, sc0.w, sc1.x, sc1.y, sc1.z, sc1.w};
-    const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+    // the metadata words: per group g the scale word scw[g] (compact: the
+    // scale codes' word g / 2) and the zero word zw[g / 2]
+    uint32_t scw[8], zw[4];
+    if constexpr (CMP) {
+        const uint4 sc0 = lds128(wbase + 2048 + 16 * r);
+        const uint4 zz = lds128(wbase + 2176 + 16 * r);
+        const uint32_t s4[4] = {sc0.x, sc0.y, sc0.z, sc0.w};
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+            scw[g] = s4[g >> 1];
+        zw[0] = zz.x; zw[1] = zz.y; zw[2] = zz.z; zw[3] = zz.w;
+    } else {
+        const uint4 sc0 = lds128(wbase + 2048 + 16 * r);
+        const uint4 sc1 = lds128(wbase + 2048 + 128 + 16 * r);
+        const uint4 zz = lds128(wbase + 2304 + 16 * r);
+        scw[0] = sc0.x; scw[1] = sc0.y; scw[2] = sc0.z; scw[3] = sc0.w;
+        scw[4] = sc1.x; scw[5] = sc1.y; scw[6] = sc1.z; scw[7] = sc1.w;
+        zw[0] = zz.x; zw[1] = zz.y; zw[2] = zz.z; zw[3] = zz.w;
+    }
     // ldmatrix.x4 row addresses: matrix lane>>3 = (step +lane>>4, k half (lane>>3)&1)
     const uint32_t xlane = xbase + (lane & 7) * XROW + 32 * (lane >> 4) + 16 * ((lane >> 3) & 1);
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -103,9 +166,6 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
             const int g = 2 * sbk + gi;
-            const uint32_t zsrc = zw[g >> 1];
-            const uint32_t zb = (uint32_t)((2 * g) & 3);  // byte of z[r][g]; z[r+8][g] follows
-            const uint32_t sp = scw[g];
             {
                 float d[NB][4];
 #pragma unroll
@@ -124,10 +184,8 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
                             mma_bf16(d[nb], a, bf[nb][2 * gi + 1][0], bf[nb][2 * gi + 1][1], d[nb]);
                     }
                 }
-                // -z as fp32: bytes [z, 0, 0, 0x4B] = 2^23 + z
-                const float nzr = 8388608.0f - __uint_as_float(prmt(zsrc, 0x4B000000u, 0x7440u + zb));
-                const float nzr8 =
-                    8388608.0f - __uint_as_float(prmt(zsrc, 0x4B000000u, 0x7440u + zb + 1));
+                float sr, sr8, nzr, nzr8;
+                group_meta<CMP>(scw[g], zw[g >> 1], g, rs, sr, sr8, nzr, nzr8);
                 if (DOTS) {
                     const int G = p.K / 32, gg = b * 8 + g;
 #pragma unroll
@@ -141,7 +199,6 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
                                 p.dots[((size_t)m * p.N + n) * G + gg] = (int32_t)rintf(dg * 4096.0f);
                         }
                 } else {
-                    const float sr = bf16lo_to_f32(sp), sr8 = bf16hi_to_f32(sp);
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) {
                         // W4A8: times the activation scale of (column, group)
@@ -180,11 +237,12 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
 // 8 / MP groups instead of once per group.  The lanes of one accumulator row
 // hold different slots of the same outputs; the flush adds them.  GS, SC: as
 // for compute_stage.
-template <int MP, bool DOTS, bool GS, bool SC, class PP>
+template <int MP, bool DOTS, bool GS, bool SC, bool CMP = false, class PP>
 __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xbase,
                                                      uint32_t sbase, uint32_t gbase, uint32_t zaddr,
                                                      int lane, float (&acc)[1][4], const PP &p,
-                                                     int tile, int b)
+                                                     int tile, int b,
+                                                     const float (&rs)[4] = {1.f, 1.f, 1.f, 1.f})
 {
     constexpr int GP = 8 / MP;  // groups per accumulator round
     const int r = lane >> 2, c2 = 2 * (lane & 3);
@@ -237,19 +295,20 @@ __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xb
                 d[e] += dacc[ai][e];
         // the groups of this lane's two columns in this round
         const int g0 = R * GP + s0, g1 = R * GP + s1;
-        const uint32_t sp0 = lds32(wbase + 2048 + ((g0 & 4) ? 128 : 0) + 16 * r + 4 * (g0 & 3));
-        const uint32_t zw0 = lds32(wbase + 2304 + 16 * r + 4 * (g0 >> 1));
-        const uint32_t sp1 = MP == 1 ? lds32(wbase + 2048 + ((g1 & 4) ? 128 : 0) + 16 * r + 4 * (g1 & 3)) : sp0;
-        const uint32_t zw1 = MP == 1 ? lds32(wbase + 2304 + 16 * r + 4 * (g1 >> 1)) : zw0;
+        // scales and negated zero points of the groups of this lane's two
+        // columns (the same group unless MP == 1), rows r and r + 8
+        uint32_t sw0, zw0;
+        group_meta_words<CMP>(wbase, r, g0, sw0, zw0);
+        float s0r, s0r8, nz0, nz08;
+        group_meta<CMP>(sw0, zw0, g0, rs, s0r, s0r8, nz0, nz08);
+        float s1r = s0r, s1r8 = s0r8, nz1 = nz0, nz18 = nz08;
+        if (MP == 1) {
+            uint32_t sw1, zw1;
+            group_meta_words<CMP>(wbase, r, g1, sw1, zw1);
+            group_meta<CMP>(sw1, zw1, g1, rs, s1r, s1r8, nz1, nz18);
+        }
         const float xs0 = __uint_as_float(lds32(sbase + m0 * SROW + 4 * g0));
         const float xs1 = __uint_as_float(lds32(sbase + m1 * SROW + 4 * g1));
-        const uint32_t zb0 = (uint32_t)((2 * g0) & 3), zb1 = (uint32_t)((2 * g1) & 3);
-        // -z as fp32: bytes [z, 0, 0, 0x4B] = 2^23 + z
-        const float nz0 = 8388608.0f - __uint_as_float(prmt(zw0, 0x4B000000u, 0x7440u + zb0));
-        const float nz08 = 8388608.0f - __uint_as_float(prmt(zw0, 0x4B000000u, 0x7440u + zb0 + 1));
-        const float nz1 = MP == 1 ? 8388608.0f - __uint_as_float(prmt(zw1, 0x4B000000u, 0x7440u + zb1)) : nz0;
-        const float nz18 =
-            MP == 1 ? 8388608.0f - __uint_as_float(prmt(zw1, 0x4B000000u, 0x7440u + zb1 + 1)) : nz08;
         if (DOTS) {
             const int G = p.K / 32;
 #pragma unroll
@@ -265,10 +324,10 @@ __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xb
             // W4A8: times the activation scale of (row of x, group)
             const float ga = GS ? __uint_as_float(lds32(gbase + m0 * SROW + 4 * g0)) : 1.f;
             const float gb = GS ? __uint_as_float(lds32(gbase + m1 * SROW + 4 * g1)) : 1.f;
-            tgt[0][0] = fmaf(bf16lo_to_f32(sp0) * ga, fmaf(nz0, xs0, d[0]), tgt[0][0]);
-            tgt[0][1] = fmaf(bf16lo_to_f32(sp1) * gb, fmaf(nz1, xs1, d[1]), tgt[0][1]);
-            tgt[0][2] = fmaf(bf16hi_to_f32(sp0) * ga, fmaf(nz08, xs0, d[2]), tgt[0][2]);
-            tgt[0][3] = fmaf(bf16hi_to_f32(sp1) * gb, fmaf(nz18, xs1, d[3]), tgt[0][3]);
+            tgt[0][0] = fmaf(s0r * ga, fmaf(nz0, xs0, d[0]), tgt[0][0]);
+            tgt[0][1] = fmaf(s1r * gb, fmaf(nz1, xs1, d[1]), tgt[0][1]);
+            tgt[0][2] = fmaf(s0r8 * ga, fmaf(nz08, xs0, d[2]), tgt[0][2]);
+            tgt[0][3] = fmaf(s1r8 * gb, fmaf(nz18, xs1, d[3]), tgt[0][3]);
         }
     }
     if (SC) {

@@ -50,6 +50,10 @@ SIGNATURES = {
     "w4a8_quantize_act_rowscale": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "w4a8_group_dots_rowscale": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, _P, _SZ, _P]),
     "w8_gemv": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w4_packed_bytes_compact": (_SZ, [_I64, _I64, _INT]),
+    "w4_pack_weights_compact": (_INT, [_P, _I64, _I64, _INT, _P, _P]),
+    "w4_unpack_weights_compact": (_INT, [_P, _I64, _I64, _INT, _P, _P, _P, _P, _P]),
+    "w4a16_gemm_compact": (_INT, [_P, _P, _P, _I64, _I64, _I64, _INT, _P]),
     "w4q_device_error": (_INT, [_U32P]),
     "w4q_selftest_wait_expiry": (_INT, [ctypes.c_uint, _P]),
 }
@@ -251,6 +255,55 @@ def w4a8_group_dots(x, packed, N, K, group=GROUP, workspace=None, stream=None):
 def w4a8_group_dots_rowscale(x, packed, N, K, group=GROUP, workspace=None, stream=None):
     """Exact int32 W4A8 group dots [M, N, K/32] (per-row activation scales)."""
     return _group_dots("w4a8_group_dots_rowscale", x, packed, N, K, group, workspace, stream)
+
+
+def packed_bytes_compact(N: int, K: int, group: int = GROUP) -> int:
+    return int(lib().w4_packed_bytes_compact(N, K, group))
+
+
+def w4_pack_weights_compact(W: torch.Tensor, group: int = GROUP, out: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """bf16 [N,K] CUDA weight -> packed uint8 buffer with the compact metadata
+    (uint8 scale / zero codes, fp16 row steps; layout of include/w4q.h)."""
+    N, K = W.shape
+    pw = _cuda(W, torch.bfloat16, "W")
+    nbytes = packed_bytes_compact(N, K, group)
+    if nbytes == 0:
+        raise W4QError("w4_pack_weights_compact", 2)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    po = _cuda(out, torch.uint8, "out")
+    _check("w4_pack_weights_compact",
+           lib().w4_pack_weights_compact(pw, N, K, group, po, _stream(stream)))
+    return out
+
+
+def w4_unpack_weights_compact(packed: torch.Tensor, N: int, K: int, group: int = GROUP,
+                              stream=None):
+    """packed -> (q u8 [N,K], scale codes u8 [N,K/32], zero codes u8 [N,K/32],
+    steps fp16 [N,2])."""
+    dev = packed.device
+    q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    sc = torch.empty(N, K // group, dtype=torch.uint8, device=dev)
+    zc = torch.empty(N, K // group, dtype=torch.uint8, device=dev)
+    st = torch.empty(N, 2, dtype=torch.float16, device=dev)
+    _check("w4_unpack_weights_compact", lib().w4_unpack_weights_compact(
+        _cuda(packed, torch.uint8, "packed"), N, K, group, q.data_ptr(), sc.data_ptr(),
+        zc.data_ptr(), st.data_ptr(), _stream(stream)))
+    return q, sc, zc, st
+
+
+def w4a16_gemm_compact(x, packed, N, K, group=GROUP, out=None, stream=None):
+    """out[M,N] = x . dequant(packed)^T with the compact metadata (M <= 8)."""
+    M = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != K:
+        raise ValueError("x must be [M, %d]" % K)
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _check("w4a16_gemm_compact", lib().w4a16_gemm_compact(
+        _cuda(x, torch.bfloat16, "x"), _cuda(packed, torch.uint8, "packed"),
+        _cuda(out, torch.bfloat16, "out"), M, N, K, group, _stream(stream)))
+    return out
 
 
 def w8_gemv(x, W, scales, out=None, stream=None):

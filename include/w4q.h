@@ -274,6 +274,60 @@ int w4a8_group_dots_rowscale(const void *x_bf16, const void *packed, int64_t M,
                              void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/* ------------------------------------------------- compact W4 metadata --- */
+
+/* The compact metadata of "test_int4_quantized_gemm.py"'s
+ * CudaCoalescedInt4Tensor: per (row, group of 32) a uint8 scale code sc and
+ * a uint8 zero code zc, per row two float16 steps ds and dz (the page's
+ * scale / zero_point and scale_step / zero_point_step).  The page prints no
+ * dequant formula; this library reads both as code x step:
+ *   scale = sc * ds,  zero = zc * dz,  dequant(q) = (q - zero) * scale,
+ * 2 bytes per group instead of the standard 3 (0.5625 bytes per weight).
+ * Quantizer, per row n, in fp64 and in this order:
+ *   s*_g = (max - min) / 15 (a constant group c: |c| / 15, or 1 if c == 0);
+ *   ds = the smallest fp16 >= max_g s*_g / 255;
+ *   sc_g = min(255, max(1, ceil(s*_g / ds)));  so scale >= s*_g;
+ *   z*_g = clamp(-min / scale_g, 0, 15);
+ *   dz = the smallest fp16 >= max_g z*_g / 255 (1.0 when every z*_g is 0);
+ *   zc_g = min(255, rint(z*_g / dz));
+ *   q = clamp(rint(w / scale_g + zero_g), 0, 15).
+ * For groups with min <= 0 <= max, |w - dequant(q)| <= scale_g / 2.  Rows
+ * whose group ranges overflow fp16 steps (max - min above ~1.2e8) or whose
+ * steps fall below the fp16 subnormal range lose that bound.
+ * Packed layout: tiles of 2304 bytes in the order of the standard layout
+ * (offset (((t/8)*(K/256) + b)*8 + t%8)*2304), each
+ *   [0, 2048)     the 4-bit codes, placed as in the standard layout;
+ *   [2048, 2176)  scale codes: (sc[16t+r][8b+g], sc[16t+r+8][8b+g]) at
+ *                 2048 + 16*r + 2*g;
+ *   [2176, 2304)  zero codes, the same pairs at 2176 + 16*r + 2*g;
+ * then, after all tiles, the fp16 pair (ds, dz) of every row n at 4*n (N
+ * padded to a multiple of 128; padding rows all zero). */
+
+/* Bytes of the compact packed buffer: ceil(N/128)*(8*(K/256)*2304 + 512);
+ * 0 when unsupported. */
+size_t w4_packed_bytes_compact(int64_t N, int64_t K, int group);
+
+/* Quantize a bf16 weight [N,K] (device) into the compact format (device,
+ * w4_packed_bytes_compact bytes, written fully).  Two launches. */
+int w4_pack_weights_compact(const void *W_bf16, int64_t N, int64_t K, int group,
+                            void *packed, void *stream);
+
+/* Inverse view: q u8 [N,K], scale codes u8 [N,K/32], zero codes u8
+ * [N,K/32], steps fp16 [N][2] (ds, dz), all device, written. */
+int w4_unpack_weights_compact(const void *packed, int64_t N, int64_t K, int group,
+                              uint8_t *q, uint8_t *scale_codes,
+                              uint8_t *zero_codes, void *steps_fp16,
+                              void *stream);
+
+/* out = x . dequant(packed)^T with the compact metadata, W4A16, 1 <= M <= 8
+ * (x, out as w4a16_gemm; packed from w4_pack_weights_compact).  Runs on the
+ * cluster kernel: per group the scale sc*ds and the zero zc*dz are formed
+ * exactly in fp32 and enter the fp32 update as in w4a16_gemm.  No
+ * workspace; W4Q_ERR_UNSUPPORTED for M > 8 or when no K split fits the
+ * kernel's shared memory (K above roughly 40960 at M <= 4). */
+int w4a16_gemm_compact(const void *x_bf16, const void *packed, void *out_bf16,
+                       int64_t M, int64_t N, int64_t K, int group, void *stream);
+
 /* ---------------------------------------------------------------- W8 --- */
 
 /* out[m,n] = bf16_RN(fp32(sum_k x[m,k] * W[n,k]) * scales[n]), one rounding
