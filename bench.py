@@ -47,16 +47,20 @@ WORKLOAD = "decode_linear_suite"
 # and the counters).  Each figure holds only for the kernel sources it was
 # taken on: the sha256 of those files, concatenated, must still match, else
 # the roofline reports traffic as null.
+W4_SOURCES = ("gemv_w4.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
+W4_DIGEST = "48cf938c77b5e9acb6e3b5d6c2f02d3ec3872486989b754aa1d5d27d45d95bc8"
+UMMA_SOURCES = ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh", "timeline.cuh")
+UMMA_DIGEST = "9def4f27dbd365548ed685a19be2cff8e1a23f7f554c3d728a58c8d73609eecc"
+CLUSTER_SOURCES = ("gemv_w4_cluster.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
+CLUSTER_DIGEST = "5184b8c05b76b7dbf8dbfe72853d8daac70ebaa9365e962a27d287875be290a5"
+W8_SOURCES = ("w8.cu", "common.cuh", "timeline.cuh")
+W8_DIGEST = "6e5d65e28a48fa02ea12def6dd430d31a50f32aae5b4c1f05273b28f176841ff"
 MEASURED_TRAFFIC = {
-    "w4a16 N=39936 K=6656 M=64": (
-        164167424, ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh"),
-        "3371cdcb57ff755b63f3836d7e7f4d5abc2b54778bad25027408690b8423977a"),
-    "w4a16 N=39936 K=6656 M=4": (
-        161165312, ("gemv_w4.cu", "common.cuh"),
-        "9647256fcdca3d2bf23a793c0c2494e1fc782aefd68a5d53469b4e69cd1288e9"),
-    "w4a16 N=39936 K=6656 M=1": (
-        160952320, ("gemv_w4.cu", "common.cuh"),
-        "9647256fcdca3d2bf23a793c0c2494e1fc782aefd68a5d53469b4e69cd1288e9"),
+    "w4a8r N=39936 K=6656 M=1": (160831744, W4_SOURCES, W4_DIGEST),
+    "w4a8r N=39936 K=6656 M=4": (161396480, W4_SOURCES, W4_DIGEST),
+    "w4a16 N=6656 K=4096 M=1": (16224512, CLUSTER_SOURCES, CLUSTER_DIGEST),
+    "w4a16 N=39936 K=6656 M=16": (161762304, UMMA_SOURCES, UMMA_DIGEST),
+    "w8 N=8192 K=8192 M=1": (67376640, W8_SOURCES, W8_DIGEST),
 }
 
 
@@ -498,15 +502,20 @@ def dominant_kernel_roofline(per_call, peaks, traffic_override=None):
     k = kern[name]
     n = len(k["calls"])
     achieved = k["bytes"] / k["us"] / 1e3
-    traffic = None
+    traffic, traffic_calls = None, []
     if traffic_override is not None:
         traffic = traffic_override
     else:
-        t = [measured_traffic(c) for c in k["calls"]]
-        if all(v is not None for v in t):
-            traffic = sum(t) / n
+        t = {c: measured_traffic(c) for c in k["calls"]}
+        traffic_calls = [c for c, v in t.items() if v is not None]
+        if traffic_calls:
+            # per launch: the mean over the calls of this kernel with a
+            # current capture (their algorithmic bytes are within 0.1% of
+            # the kernel's mean)
+            traffic = sum(t[c] for c in traffic_calls) / len(traffic_calls)
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "traffic_calls": traffic_calls,
             "kernel": name, "share_of_step": round(k["share"], 4), "launches_per_step": n,
             "calls": k["calls"], "algorithmic_bytes_per_launch": round(k["bytes"] / n),
             "us_per_launch": round(k["us"] / n, 3), "peak_source": peaks["source"]}
