@@ -3,13 +3,46 @@
 // device memory or synchronizes (except w4q_device_error).
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "w4q.h"
 
 namespace w4q {
 bool w8_supported(int M, int K);
+
+// The driver's unique id of the context current on this thread, 0 if there is
+// none yet or the driver cannot say.  The two driver calls are resolved once
+// through the runtime, so the library needs no link to libcuda.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static const GetCurrent get_current = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                           cudaSuccess && q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<GetCurrent>(f)
+                   : nullptr;
+    }();
+    static const GetId get_id = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                           cudaSuccess && q == cudaDriverEntryPointSuccess
+                   ? reinterpret_cast<GetId>(f)
+                   : nullptr;
+    }();
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&c) != CUDA_SUCCESS || c == nullptr ||
+        get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
 }
+}  // namespace w4q
 
 namespace {
 
@@ -20,6 +53,7 @@ constexpr int MAX_DEV = 64;
 std::mutex g_mu;
 int g_sm_count[MAX_DEV];
 unsigned *g_err_ptr[MAX_DEV];
+unsigned long long g_err_ctx[MAX_DEV];  // context the cached address belongs to
 
 int current_device()
 {
@@ -44,11 +78,13 @@ int sm_count(int dev)
 unsigned *error_word(int dev)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_err_ptr[dev] == nullptr) {
+    const unsigned long long ctx = w4q::current_context_id();
+    if (g_err_ptr[dev] == nullptr || ctx == 0 || ctx != g_err_ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess)
             return nullptr;
         g_err_ptr[dev] = static_cast<unsigned *>(p);
+        g_err_ctx[dev] = w4q::current_context_id();
     }
     return g_err_ptr[dev];
 }

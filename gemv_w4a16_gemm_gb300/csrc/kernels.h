@@ -78,6 +78,7 @@ cudaError_t launch_act_quant_i8(const void *x, int M, int K, int8_t *xq, float *
 // --- per-device state kept by api.cu
 int device_sm_count(int dev);
 unsigned *device_error_word(int dev);  // nullptr if the symbol lookup failed
+unsigned long long current_context_id();  // 0 if no context is current
 
 // --- W8 GEMV (w8.cu)
 cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *out, int M, int N,

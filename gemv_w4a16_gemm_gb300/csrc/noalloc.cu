@@ -30,17 +30,21 @@ static __device__ __align__(256) unsigned char g_scratch[STATIC_SCRATCH_BYTES];
 
 constexpr int MAX_DEV = 64;
 std::mutex g_mu;
-void *g_scratch_addr[MAX_DEV];  // device address of g_scratch, per device
+void *g_scratch_addr[MAX_DEV];               // device address of g_scratch, per device
+unsigned long long g_scratch_ctx[MAX_DEV];    // the context that address belongs to
 
-// Looks the array up once per device, with that device current.
+// Looks the array up with that device current, again whenever the current
+// context is not the one the cached address came from (after a device reset).
 void *scratch_address(int dev)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    const unsigned long long ctx = w4q::current_context_id();
+    if (g_scratch_addr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr)
             return nullptr;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = w4q::current_context_id();
     }
     return g_scratch_addr[dev];
 }

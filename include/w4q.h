@@ -22,7 +22,13 @@
  * Conventions (every entry point):
  *   - Pointers marked "device" are device pointers owned by the caller; the
  *     library never frees, retains or allocates memory, and keeps no state
- *     except a per-device SM-count cache and one device-side error word.
+ *     except a per-device SM-count cache and two module variables (the
+ *     device-side error word and the no-allocation scratch array).  Their
+ *     device addresses are cached together with the id of the CUDA context
+ *     they were looked up in and looked up again when another context is
+ *     current, so calls after cudaDeviceReset (or any teardown and re-creation
+ *     of the context) use the new context's copies; an error word set in a
+ *     context that was torn down is lost with it.
  *   - Device pointers must be 16-byte aligned, else W4Q_ERR_MISALIGNED.
  *     Outputs must not alias inputs.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*,
