@@ -69,6 +69,26 @@ def test_every_legal_split_matches(cuda):
                          "M=%d split=%d" % (M, split))
 
 
+def test_stream_k_every_m(cuda):
+    # 8448 x 6656 under explicit stream-K: 1716 units over two CTA slots per
+    # SM, so most tile groups are split between CTAs and summed through the
+    # split-K partials.  Every output is compared (the output starts as NaN),
+    # and repeated calls must agree bitwise (the parts are summed in a fixed
+    # order, whichever CTA arrives last).
+    N, K = 8448, 6656
+    W, q, s, z = quantized(N, K, seed=77)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in range(1, 9):
+        x = workloads.activation(M, K, seed=300 + M)
+        xd = x.to(cuda)
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=cuda)
+        w4q.w4a16_gemm(xd, packed, N, K, split_k=0, out=out)
+        assert_close(out, oracle.w4a16(x, q, s, z), "stream-K M=%d" % M)
+        for _ in range(3):
+            assert torch.equal(w4q.w4a16_gemm(xd, packed, N, K, split_k=0), out), M
+    assert w4q.device_error() == 0
+
+
 def test_illegal_split_is_rejected(cuda):
     N, K = 256, 768
     W = workloads.w4_weight(N, K, seed=0)

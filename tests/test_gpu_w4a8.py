@@ -94,6 +94,13 @@ def test_every_legal_split_matches(cuda):
         _check(cuda, N, K, (1, 4), split_k=split, seed_w=91)
 
 
+def test_stream_k(cuda):
+    # explicit stream-K on 8448 x 6656 (groups split between CTAs): every
+    # output against the oracle
+    _check(cuda, 8448, 6656, (1, 2, 4, 7), split_k=0, seed_w=98)
+    assert w4q.device_error() == 0
+
+
 def test_zero_rows_and_zero_input(cuda):
     N, K = 128, 512
     W, q, s, z = quantized(N, K, seed=4)

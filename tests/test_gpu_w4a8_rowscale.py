@@ -93,6 +93,20 @@ def test_every_legal_split_matches(cuda):
         _check(cuda, N, K, (1, 4), split_k=split, seed_w=93)
 
 
+def test_stream_k(cuda):
+    # explicit stream-K on 8448 x 6656 (groups split between CTAs): every
+    # output against the oracle, repeated calls bitwise equal
+    N, K = 8448, 6656
+    _check(cuda, N, K, (1, 2, 3, 4, 8), split_k=0, seed_w=96)
+    W = workloads.w4_weight(N, K, 96)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    x = workloads.activation(3, K, seed=97).to(cuda)
+    ref = w4q.w4a8_gemm_rowscale(x, packed, N, K, split_k=0)
+    for _ in range(3):
+        assert torch.equal(w4q.w4a8_gemm_rowscale(x, packed, N, K, split_k=0), ref)
+    assert w4q.device_error() == 0
+
+
 def test_row_max_in_another_slice_of_the_cluster(cuda):
     # per-row scale with the row's max in a different K slice for each row,
     # under every cluster split: the slices' maxima must be combined
