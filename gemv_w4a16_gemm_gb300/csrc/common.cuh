@@ -246,4 +246,39 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// The W4A8 activation code of eight values: v[j] <- clamp(rint(fp32(v[j] /
+// sx)), -127, 127), with sx = fp32(a / 127) for the max |v| a (> 0) of
+// their group or row, so |v / sx| <= 127 (1 + 2^-23).  Computed as
+// rint(v * r) with r = fp32(1 / sx): r and the product each round once,
+// so |v * r - v / sx| < 2^-16 and |fp32(v / sx) - v / sx| < 2^-17, and
+// the two round to the same integer unless v * r lies within 2^-15 of a
+// half-integer.  There (|v * r - rint(v * r)| > 1/2 - 2^-14 is the test,
+// with margin), and for a tiny sx whose reciprocal would overflow, the
+// correctly rounded quotient decides.
+__device__ __forceinline__ void act_code8(float (&v)[8], float sx)
+{
+    const float r = __frcp_rn(sx);
+    const bool tiny = !(sx >= 0x1p-125f);
+    constexpr float NEAR = 0.5f - 0x1p-14f;
+    float q[8];
+    bool near = tiny;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float y = v[j] * r;
+        q[j] = rintf(y);
+        near |= fabsf(y - q[j]) > NEAR;
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float y = v[j] * r;
+            if (tiny || fabsf(y - rintf(y)) > NEAR)
+                q[j] = rintf(__fdiv_rn(v[j], sx));
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        v[j] = fminf(fmaxf(q[j], -127.f), 127.f);
+}
+
 }  // namespace w4q

@@ -18,7 +18,7 @@
 //     moves a stage's rows):
 //       W4A16:  per row and 256-column super-block, x' = x * 2^sigma (the
 //               W4A16 rule below), X', and the row factor c;
-//       W4A8:   sx = fp32(max|x| / 127) per (row, group of 32),
+//       W4A8:   sx = fp32(max|x| / 127) per (row, group of 32) or per row,
 //               xq = clamp(rint(fp32(x / sx))), x' = xq * 2^121 (2^117 on
 //               upper halves), X'[g] = 2^-12 * sum xq (exact), group scale
 //               sx * 2^12.
@@ -43,7 +43,7 @@
 //         and a kernel boundary off the critical path of the call.  At
 //         M >= 3 the preparation would cost the producer warp's scheduler
 //         more than the consumers sharing it can give, so the prologue does
-//         it.
+//         it; so it would for W4A8 at any M (its quantizer's divisions).
 //       * Consumer warp w owns row tile w of the CTA's 128-row tile group.
 //         A lane's 16 bytes of a sub-block hold its A fragments of four
 //         m16n8k16 MMAs; masking a word with 0x000F000F / 0x00F000F0 turns
@@ -562,6 +562,7 @@ __device__ __forceinline__ float row_absmax(const __nv_bfloat16 *__restrict__ x,
     __shared__ uint32_t wmax[32];
     const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)m * K);
     uint32_t h = 0u;
+#pragma unroll 4
     for (int j = threadIdx.x; j < K / 8; j += blockDim.x) {
         const uint4 v = row[j];
         h = __vmaxu2(h, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
@@ -605,10 +606,10 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
     const int n8 = K / 8;
     const int i = blockIdx.y * PREP_THREADS + threadIdx.x;
     const bool live = i < n8;
+    const uint4 raw = live ? row[i] : make_uint4(0u, 0u, 0u, 0u);  // before the row pass: one round trip
     const float arow = ROW ? row_absmax(x, m, K) : 0.f;
     float v[8];
     if (live) {
-        const uint4 raw = row[i];
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -644,9 +645,13 @@ __global__ void __launch_bounds__(PREP_THREADS) act_prep_kernel(
         if (ROW)
             a = arow;
         const float sxg = __fdiv_rn(a, 127.0f);
+        if (a == 0.f) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sxg)), -127.f), 127.f);
+            for (int j = 0; j < 8; ++j)
+                v[j] = 0.f;
+        } else {
+            act_code8(v, sxg);
+        }
         const int g = i / 4;  // x 2^12: the group dots come out of the MMA scaled by 2^-12
         if (live && (i & 3) == 0)
             gscale[((size_t)(g / 8) * M + m) * 8 + (g % 8)] = sxg * 4096.0f;
@@ -716,11 +721,16 @@ __global__ void __launch_bounds__(512) act_quant_i8_kernel(const __nv_bfloat16 *
             if (ROW ? i == 0 : (i & 3) == 0)
                 sx[ROW ? (size_t)m : (size_t)m * (K / 32) + i / 4] = s;
             uint32_t q[2] = {0u, 0u};
+            if (a == 0.f) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float qf = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(f[j], s)), -127.f), 127.f);
-                q[j / 4] |= (uint32_t)(uint8_t)(int8_t)qf << (8 * (j % 4));
+                for (int j = 0; j < 8; ++j)
+                    f[j] = 0.f;
+            } else {
+                act_code8(f, s);
             }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                q[j / 4] |= (uint32_t)(uint8_t)(int8_t)f[j] << (8 * (j % 4));
             reinterpret_cast<uint2 *>(xq + (size_t)m * K)[i] = make_uint2(q[0], q[1]);
         }
     }

@@ -182,12 +182,17 @@ __device__ __forceinline__ void prep_stage_a8(const uint4 (&raw)[MP], int M, int
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         }
         const float sx = __fdiv_rn(a, 127.0f);
+        if (a == 0.f) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = 0.f;
+        } else {
+            act_code8(v, sx);
+        }
         float part = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            v[j] = (a == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(v[j], sx)), -127.f), 127.f);
+        for (int j = 0; j < 8; ++j)
             part += v[j];
-        }
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         // |xq| <= 127 has at most 7 significant bits: xq * 2^sh is exact in bf16

@@ -31,6 +31,22 @@ def test_activation_quantizer_bit_exact(cuda, M, K):
     assert np.array_equal(xq.cpu().numpy(), oxq)
 
 
+def test_activation_quantizer_every_bf16_value(cuda):
+    # every positive bf16 magnitude, in groups of 32 whose maxima vary: the
+    # int8 codes and per-group scales bit for bit
+    K = 32768
+    bits = np.arange(1, K + 1, dtype=np.uint32)
+    v = (bits << 16).view(np.float32)
+    v = np.where(np.isfinite(v), v, np.float32(1.0))
+    v = np.where(np.arange(K) % 3 == 0, -v, v)
+    rows = [v, v[::-1].copy(), np.roll(v, 7)]
+    x = torch.from_numpy(np.stack(rows)).to(torch.bfloat16)
+    xq, sx = w4q.w4a8_quantize_act(x.to(cuda))
+    oxq, osx = oracle.act_quant(x, K)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), oxq), np.argwhere(xq.cpu().numpy() != oxq)[:5]
+
+
 def test_activation_quantizer_ties(cuda):
     K = 256
     vals = [127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 3.0, -127.0]

@@ -32,6 +32,33 @@ def test_activation_quantizer_bit_exact(cuda, M, K):
     assert np.array_equal(xq.cpu().numpy(), oxq)
 
 
+def _all_bf16_rows(maxima):
+    """One row per maximum a: a, then every positive finite bf16 number up to
+    a (each larger one replaced by a, the row padded with a), signs
+    alternating.  K = 32768."""
+    K = 32768
+    bits = np.arange(1, 0x7F80, dtype=np.uint32)      # the positive finite bf16 numbers
+    vals = (bits << 16).view(np.float32)
+    vals = np.concatenate([vals, np.full(K - 1 - vals.size, np.inf, np.float32)])
+    rows = []
+    for a in maxima:
+        a = float(torch.tensor(a, dtype=torch.bfloat16))
+        v = np.minimum(vals, np.float32(a))
+        v = np.where(np.arange(v.size) % 2 == 0, v, -v)
+        rows.append(np.concatenate([[np.float32(a)], v]))
+    return torch.from_numpy(np.stack(rows).astype(np.float32)).to(torch.bfloat16), K
+
+
+def test_activation_quantizer_every_bf16_value(cuda):
+    # every positive bf16 magnitude under several row maxima (quotients near
+    # every half-integer included): the int8 codes and scales bit for bit
+    x, K = _all_bf16_rows((127.0, 1.0, 3.7e-3, 300.0, 1e30, 2.0 ** -120, 0.4375, 6.02e4))
+    xq, sx = w4q.w4a8_quantize_act_rowscale(x.to(cuda))
+    oxq, osx = oracle.act_quant_row(x, K)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), osx.view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), oxq), np.argwhere(xq.cpu().numpy() != oxq)[:5]
+
+
 def test_activation_quantizer_ties(cuda):
     # max |x| = 127 -> sx = 1 exactly; .5 ties round to even
     K = 512
