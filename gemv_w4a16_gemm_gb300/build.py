@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libw4q.so")
 SOURCES = ("api.cu", "pack.cu", "pack_compact.cu", "gemv_w4.cu", "gemv_w4_cluster.cu",
-           "gemv_w4_umma.cu", "w8.cu", "noalloc.cu", "selftest.cu")
+           "gemv_w4_umma.cu", "w8.cu", "gemv_w8_umma.cu", "noalloc.cu", "selftest.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -10,7 +10,6 @@
 #include "w4q.h"
 
 namespace w4q {
-bool w8_supported(int M, int K);
 
 // The driver's unique id of the context current on this thread, 0 if there is
 // none yet or the driver cannot say.  The two driver calls are resolved once
@@ -434,6 +433,58 @@ int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16, void *
         return W4Q_ERR_CUDA;
     cudaError_t e = w4q::launch_w8(x_bf16, W, scales_bf16, out_bf16, (int)M, (int)N, (int)K,
                                    sm_count(dev), err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
+}
+
+size_t w8_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || M > 64 || N > MAX_N || K > MAX_K || K % 16 != 0)
+        return 0;
+    if (w4q::w8_supported((int)M, (int)K))
+        return 0;  // the CUDA-core kernel: no workspace
+    const int dev = current_device();
+    if (dev < 0)
+        return 0;
+    return w4q::w8_tc_workspace((int)M, (int)N, (int)K, sm_count(dev));
+}
+
+int w8_kernel_launches(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || M > 64 || N > MAX_N || K > MAX_K || K % 16 != 0)
+        return 0;
+    if (w4q::w8_supported((int)M, (int)K))
+        return 1;
+    const int dev = current_device();
+    if (dev < 0)
+        return 0;
+    return w4q::w8_tc_launches((int)M, (int)N, (int)K, sm_count(dev));
+}
+
+int w8_gemm(const void *x_bf16, const int8_t *W, const void *scales_bf16, void *out_bf16, int64_t M,
+            int64_t N, int64_t K, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (x_bf16 == nullptr || W == nullptr || scales_bf16 == nullptr || out_bf16 == nullptr)
+        return W4Q_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || K % 16 != 0)
+        return W4Q_ERR_INVALID_ARG;
+    if (M > 64 || N > MAX_N || K > MAX_K)
+        return W4Q_ERR_UNSUPPORTED;
+    if (w4q::w8_supported((int)M, (int)K))
+        return w8_gemv(x_bf16, W, scales_bf16, out_bf16, M, N, K, stream);
+    if (!aligned16(x_bf16) || !aligned16(W) || !aligned16(scales_bf16) || !aligned16(out_bf16) ||
+        (workspace != nullptr && !aligned16(workspace)))
+        return W4Q_ERR_MISALIGNED;
+    const int dev = current_device();
+    if (dev < 0)
+        return W4Q_ERR_CUDA;
+    const size_t need = w4q::w8_tc_workspace((int)M, (int)N, (int)K, sm_count(dev));
+    if (workspace == nullptr || workspace_bytes < need)
+        return W4Q_ERR_WORKSPACE;
+    unsigned *err = error_word(dev);
+    if (err == nullptr)
+        return W4Q_ERR_CUDA;
+    cudaError_t e = w4q::launch_w8_tc(x_bf16, W, scales_bf16, out_bf16, (int)M, (int)N, (int)K,
+                                      sm_count(dev), workspace, err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
 }
 

@@ -168,6 +168,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// 2-D tiled bulk copy global -> this CTA's shared memory through a tensor
+// map (a __grid_constant__ kernel parameter), completing the box's bytes on
+// the mbarrier.  (x, y): the box's first element (x innermost, its byte
+// offset a multiple of 16); parts of the box outside the tensor read zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+                 : "memory");
+}
+
 // ------------------------------------------------- programmatic launches
 
 // Let the next kernel in the stream (launched with programmatic stream

@@ -80,8 +80,15 @@ int device_sm_count(int dev);
 unsigned *device_error_word(int dev);  // nullptr if the symbol lookup failed
 unsigned long long current_context_id();  // 0 if no context is current
 
-// --- W8 GEMV (w8.cu)
+// --- W8 GEMV (w8.cu): CUDA cores, 1 <= M <= 4, K <= 16384, no workspace
 cudaError_t launch_w8(const void *x, const int8_t *W, const void *scales, void *out, int M, int N,
                       int K, int sm_count, unsigned *err, cudaStream_t stream);
+bool w8_supported(int M, int K);
+
+// --- W8 on the tcgen05 tensor core, any 1 <= M <= 64 (gemv_w8_umma.cu)
+size_t w8_tc_workspace(int M, int N, int K, int sm_count);
+int w8_tc_launches(int M, int N, int K, int sm_count);
+cudaError_t launch_w8_tc(const void *x, const int8_t *W, const void *scales, void *out, int M, int N,
+                         int K, int sm_count, void *workspace, unsigned *err, cudaStream_t stream);
 
 }  // namespace w4q

@@ -120,6 +120,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
+// The same with fp16 A and B.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
+{
+    return (1u << 4)                          // D format: f32 (A, B format 0: f16)
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte
 // swizzle layout: 8-row x 128-byte atoms (the 16-byte chunk c of row r
 // stored at chunk c ^ r), atoms of consecutive 8-row groups 1024 bytes

@@ -50,6 +50,9 @@ SIGNATURES = {
     "w4a8_quantize_act_rowscale": (_INT, [_P, _I64, _I64, _P, _P, _P]),
     "w4a8_group_dots_rowscale": (_INT, [_P, _P, _I64, _I64, _I64, _INT, _P, _P, _SZ, _P]),
     "w8_gemv": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "w8_gemm": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "w8_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "w8_kernel_launches": (_INT, [_I64, _I64, _I64]),
     "w4_packed_bytes_compact": (_SZ, [_I64, _I64, _INT]),
     "w4_pack_weights_compact": (_INT, [_P, _I64, _I64, _INT, _P, _P]),
     "w4_unpack_weights_compact": (_INT, [_P, _I64, _I64, _INT, _P, _P, _P, _P, _P]),
@@ -317,6 +320,34 @@ def w8_gemv(x, W, scales, out=None, stream=None):
         out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
     po = _cuda(out, torch.bfloat16, "out")
     _check("w8_gemv", lib().w8_gemv(px, pw, ps, po, M, N, K, _stream(stream)))
+    return out
+
+
+def w8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().w8_workspace_bytes(M, N, K))
+
+
+def w8_kernel_launches(M: int, N: int, K: int) -> int:
+    return int(lib().w8_kernel_launches(M, N, K))
+
+
+def w8_gemm(x, W, scales, out=None, workspace=None, stream=None):
+    """w8_gemv for 1 <= M <= 64 (the tensor-core path needs a workspace;
+    one is allocated when none is given)."""
+    M, K = x.shape
+    N = W.shape[0]
+    px = _cuda(x, torch.bfloat16, "x")
+    pw = _cuda(W, torch.int8, "W")
+    ps = _cuda(scales, torch.bfloat16, "scales")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    po = _cuda(out, torch.bfloat16, "out")
+    need = w8_workspace_bytes(M, N, K)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    pws = _cuda(workspace, torch.uint8, "workspace") if workspace is not None else None
+    nbytes = workspace.numel() if workspace is not None else 0
+    _check("w8_gemm", lib().w8_gemm(px, pw, ps, po, M, N, K, pws, nbytes, _stream(stream)))
     return out
 
 

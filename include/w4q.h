@@ -347,6 +347,33 @@ int w4a16_gemm_compact(const void *x_bf16, const void *packed, void *out_bf16,
 int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16,
             void *out_bf16, int64_t M, int64_t N, int64_t K, void *stream);
 
+/* The same operation for 1 <= M <= 64 ("gpt-fast issue #114": its open
+ * question of batch sizes above one).  x, W, scales, out as w8_gemv; K a
+ * positive multiple of 16 up to 2^20, N up to 2^24.
+ *   workspace        device, >= w8_workspace_bytes(M, N, K) bytes, 16-byte
+ *                    aligned, owned by the caller; may be NULL when that is 0
+ * Calls w8_gemv supports run there (no workspace).  The others run on the
+ * tcgen05 tensor core in fp16 with fp32 accumulation: every int8 weight is an
+ * fp16 number exactly, and each row m of x is scaled by a power of two
+ * 2^sigma_m (max |x[m]| 2^sigma in [2^14, 2^15)), which keeps every bf16
+ * value down to 2^-28 of the row's max exact in fp16; the result is
+ * bf16_RN((acc 2^-sigma_m) * scales[n]).  Two or three launches (see
+ * w8_kernel_launches); W4Q_ERR_WORKSPACE when the workspace is missing or
+ * too small. */
+int w8_gemm(const void *x_bf16, const int8_t *W, const void *scales_bf16,
+            void *out_bf16, int64_t M, int64_t N, int64_t K, void *workspace,
+            size_t workspace_bytes, void *stream);
+
+/* Workspace bytes w8_gemm needs for these sizes on the current device (0
+ * when w8_gemv serves the call or the sizes are invalid). */
+size_t w8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Kernel launches of one w8_gemm call (1 for the CUDA-core kernel; 2 or 3
+ * on the tensor core: activation preparation, the main kernel and, when a
+ * row pair's K is split between CTAs, the partial-sum launch); 0 for
+ * invalid sizes. */
+int w8_kernel_launches(int64_t M, int64_t N, int64_t K);
+
 /* ------------------------------------------------------------ status --- */
 
 /* Read and clear the device-side error word of the current device (set by
