@@ -100,6 +100,8 @@ def step_calls():
     for (N, K) in workloads.TC_SHAPES:
         for M in workloads.TC_MS:
             calls.append(("w4a16", N, K, M))
+    for M in workloads.W8_TC_MS:
+        calls.append(("w8", workloads.W8_GEMV["N"], workloads.W8_GEMV["K"], M))
     return calls
 
 
@@ -125,7 +127,7 @@ def kernel_name(kind, M, launches=None):
     """The call's main kernel; `launches` (the library's launch count for the
     call) tells the one-launch cluster kernel from the stream-K kernel."""
     if kind == "w8":
-        return "w8_kernel<M=%d>" % M
+        return "w8_kernel<M=%d>" % M if launches == 1 else "w8_umma_kernel<NP=%d>" % ((M + 15) // 16 * 16)
     if kind == "w4a16" and M >= 9:
         return "w4_umma_kernel<NP=%d>" % ((M + 15) // 16 * 16)
     if kind == "w4a16c":
@@ -241,7 +243,10 @@ class Suite:
             self.x[i] = x.to(dev)
             self.out[i] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             self.out_host[i] = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
-            if kind not in ("w8", "w4a16c"):
+            if kind == "w8":
+                self.ws[i] = torch.empty(max(w4q.w8_workspace_bytes(M, N, K), 16),
+                                         dtype=torch.uint8, device=dev)
+            elif kind != "w4a16c":
                 nbytes = max(w4q.workspace_bytes(M, N, K), 16)
                 self.ws[i] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
@@ -259,7 +264,7 @@ class Suite:
         x = self.x[i] if x is None else x
         out = self.out[i] if out is None else out
         if kind == "w8":
-            self.w4q.w8_gemv(x, w, self.extra[self.wkey(kind, N, K)], out=out)
+            self.w4q.w8_gemm(x, w, self.extra[self.wkey(kind, N, K)], out=out, workspace=self.ws[i])
         elif kind == "w4a16":
             self.w4q.w4a16_gemm(x, w, N, K, out=out, workspace=self.ws[i])
         elif kind == "w4a8r":
@@ -269,12 +274,16 @@ class Suite:
         else:
             self.w4q.w4a8_gemm(x, w, N, K, out=out, workspace=self.ws[i])
 
+    def call_launches(self, kind, N, K, M):
+        """Kernels the library launches for one call."""
+        if kind == "w4a16c":
+            return 1
+        if kind == "w8":
+            return self.w4q.w8_kernel_launches(M, N, K)
+        return self.w4q.kernel_launches(M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
+
     def launches_per_step(self):
-        n = 0
-        for kind, N, K, M in self.calls:
-            n += 1 if kind in ("w8", "w4a16c") else self.w4q.kernel_launches(
-                M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
-        return n
+        return sum(self.call_launches(*c) for c in self.calls)
 
     def step_copy_index(self, i):
         """Distinct copy per call within a step (calls of one shape rotate)."""
@@ -316,8 +325,7 @@ def measure_calls(suite, reps=3):
             b.synchronize()
             times.append(a.elapsed_time(b) * 1e3 / R)
         us = statistics.median(times[1:])
-        launches = None if kind in ("w8", "w4a16c") else suite.w4q.kernel_launches(
-            M, N, K, {"w4a16": False, "w4a8": "group", "w4a8r": "row"}[kind])
+        launches = suite.call_launches(kind, N, K, M)
         res.append(dict(call=call_label(kind, N, K, M), kind=kind, N=N, K=K, M=M,
                         kernel=kernel_name(kind, M, launches), us=us,
                         weight_gbs=weight_bytes(kind, N, K) / us / 1e3,
@@ -446,7 +454,7 @@ def run_gpu(args, rank, world, dist):
                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                "frac": round(2.0 * c["M"] * c["N"] * c["K"] / c["us"] / 1e6 / peaks["bf16_tflops"], 4),
                "peak_source": peaks["source"].replace("copy", "cuBLAS bf16 GEMM, burst")}
-              for c in per_call if c["kind"] == "w4a16" and c["M"] >= 9]
+              for c in per_call if (c["kind"] == "w4a16" and c["M"] >= 9) or "umma" in c["kernel"]]
     value = replica_value(world, step_weight, ms)
     w8 = next(c for c in per_call if c["kind"] == "w8")
     clocks = clk.summary()
@@ -678,7 +686,8 @@ def profile_call(spec, launches):
     if kind == "w8":
         W, sc, _ = workloads.w8_inputs(N=N, K=K, M=1)
         W, sc = W.to(dev), sc.to(dev)
-        fn = lambda: w4q.w8_gemv(x, W, sc)  # noqa: E731
+        ws = torch.empty(max(w4q.w8_workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
+        fn = lambda: w4q.w8_gemm(x, W, sc, workspace=ws)  # noqa: E731
     else:
         if kind == "w4a16c":
             packed = w4q.w4_pack_weights_compact(workloads.w4_weight(N, K).to(dev))

@@ -436,11 +436,21 @@ int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16, void *
     return e == cudaSuccess ? W4Q_OK : W4Q_ERR_CUDA;
 }
 
+// W8 calls up to this M (and K within its range) run on the CUDA-core
+// kernel (w8.cu), the others on the tensor core (gemv_w8_umma.cu).
+#ifndef W4Q_W8_CC_MAX_M
+#define W4Q_W8_CC_MAX_M 1
+#endif
+static bool w8_on_cuda_cores(int64_t M, int64_t K)
+{
+    return M <= W4Q_W8_CC_MAX_M && w4q::w8_supported((int)M, (int)K);
+}
+
 size_t w8_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0 || M > 64 || N > MAX_N || K > MAX_K || K % 16 != 0)
         return 0;
-    if (w4q::w8_supported((int)M, (int)K))
+    if (w8_on_cuda_cores(M, K))
         return 0;  // the CUDA-core kernel: no workspace
     const int dev = current_device();
     if (dev < 0)
@@ -452,7 +462,7 @@ int w8_kernel_launches(int64_t M, int64_t N, int64_t K)
 {
     if (M <= 0 || N <= 0 || K <= 0 || M > 64 || N > MAX_N || K > MAX_K || K % 16 != 0)
         return 0;
-    if (w4q::w8_supported((int)M, (int)K))
+    if (w8_on_cuda_cores(M, K))
         return 1;
     const int dev = current_device();
     if (dev < 0)
@@ -469,7 +479,7 @@ int w8_gemm(const void *x_bf16, const int8_t *W, const void *scales_bf16, void *
         return W4Q_ERR_INVALID_ARG;
     if (M > 64 || N > MAX_N || K > MAX_K)
         return W4Q_ERR_UNSUPPORTED;
-    if (w4q::w8_supported((int)M, (int)K))
+    if (w8_on_cuda_cores(M, K))
         return w8_gemv(x_bf16, W, scales_bf16, out_bf16, M, N, K, stream);
     if (!aligned16(x_bf16) || !aligned16(W) || !aligned16(scales_bf16) || !aligned16(out_bf16) ||
         (workspace != nullptr && !aligned16(workspace)))

@@ -37,6 +37,8 @@ W4A8_SHAPE = (39936, 6656)
 W4A8_MS = (1, 2, 3, 4)
 TC_SHAPES = ((39936, 6656), (6656, 19968), (1536, 512))
 TC_MS = (16, 64)
+# W8 at the skinny-GEMM sizes (on the tensor core)
+W8_TC_MS = (16, 64)
 
 
 def _gen(seed: int) -> torch.Generator:
