@@ -59,6 +59,13 @@
 #define W4Q_RING_WAIT mbar_wait_sleep
 #endif
 
+// Largest rows-per-slot count at which consumers take ring stages two at a
+// time (measured: a gain at one row per slot, a loss at two on 6656 x 4096 and
+// 8448 x 6656).
+#ifndef W4Q_CL_PAIR_MP
+#define W4Q_CL_PAIR_MP 1
+#endif
+
 namespace w4q {
 
 namespace {
@@ -442,10 +449,10 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * (i % R));
         };
-        if constexpr (MP <= 2) {
+        if constexpr (MP <= W4Q_CL_PAIR_MP) {
             // Two stages at a time when both are in the ring, so that their
-            // MMA chains interleave (measured: 17.96 -> 17.31 us on 6656 x
-            // 19968 at M = 1; at MP = 4 the doubled register state made it
+            // MMA chains interleave (measured at M = 1: 18.1 -> 17.6 us on
+            // 6656 x 19968; at MP = 4 the doubled register state made it
             // slower).
             int i = 0;
             for (; i + 1 < S; i += 2) {
