@@ -214,6 +214,10 @@ __global__ void __launch_bounds__(W8_THREADS, 1) w8_umma_kernel(const __grid_con
             int gp = gp_first, b = b_first, issued = 0;
             for (int i = 0; i < n_iter; ++i) {
                 const int slot = i % SW;
+#ifdef W4Q_UMMA_PREFETCH
+                if (i == W4Q_UMMA_PREFETCH)
+                    pdl_wait();
+#endif
                 if (i >= SW && !mbar_wait_sleep(wempty0 + 8 * slot, (uint32_t)((i / SW) - 1) & 1u)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
@@ -532,6 +536,9 @@ constexpr int W8_FIX_ROWS = 8;
 
 __global__ void __launch_bounds__(W8_PAIR_ROWS) w8_umma_fixup_kernel(const __grid_constant__ W8UParams p)
 {
+    // The next call's preparation may launch and wait beside these blocks
+    // (measured on 6656 x 19968 at M = 16: 31.1 -> 29.4 us per call).
+    pdl_launch_dependents();
     pdl_wait();
     const int gp = blockIdx.x, m0 = blockIdx.y * W8_FIX_ROWS, row = threadIdx.x;
     const long long gb = (long long)gp * p.KB, ge = gb + p.KB;

@@ -42,7 +42,7 @@ EVENTS = {
     30: "w8 kernel: CTA start", 31: "w8: waited", 32: "w8: last stage done",
     40: "tcgen05 kernel: CTA start", 41: "tcgen05: x producer waited", 42: "tcgen05: CTA end",
     44: "prologue (B operand): start", 45: "prologue (B operand): waited",
-    47: "partial-sum launch: waited",
+    47: "partial-sum launch: waited", 48: "partial-sum launch: block end",
 }
 END_EVENTS = (16, 25, 32, 42)
 
@@ -126,6 +126,7 @@ def run(specs, R=20):
         if kind == "w8":
             W, sc, _ = workloads.w8_inputs(N=N, K=K, M=1)
             base, sc = W.to(dev), sc.to(dev)
+            ws = torch.empty(max(w4q.w8_workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=dev)
         else:
             base = w4q.w4_pack_weights(workloads.w4_weight(N, K).to(dev))
             ws = torch.empty(max(w4q.workspace_bytes(M, N, K, split_k=split), 16),
@@ -138,7 +139,7 @@ def run(specs, R=20):
             for r in range(R):
                 w = pool[r % len(pool)]
                 if kind == "w8":
-                    w4q.w8_gemv(x, w, sc, out=out)
+                    w4q.w8_gemm(x, w, sc, out=out, workspace=ws)
                 else:
                     op(x, w, N, K, split_k=split, out=out, workspace=ws)
 
