@@ -237,10 +237,6 @@ __global__ void __launch_bounds__(UT_THREADS, 1) w4_umma_kernel(const UParams p)
             int gp = gp_first, b = b_first, issued = 0;
             for (int i = 0; i < n_iter; ++i) {
                 const int slot = i % SW;
-#ifdef W4Q_UMMA_PREFETCH
-                if (i == W4Q_UMMA_PREFETCH)
-                    pdl_wait();
-#endif
                 if (i >= SW && !mbar_wait_sleep(wempty0 + 8 * slot, (uint32_t)((i / SW) - 1) & 1u)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
@@ -572,17 +568,11 @@ __global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 
 // sum, so the launch is about one wave of a few L2 round trips.  Launched
 // behind the main kernel with programmatic dependent launch;
 // griddepcontrol.wait holds it until the main kernel has finished.
-#ifndef W4Q_FIX_ROWS
-#define W4Q_FIX_ROWS 8
-#endif
-#ifndef W4Q_FIX_CHUNK
-#define W4Q_FIX_CHUNK 4
-#endif
-constexpr int UT_FIX_ROWS = W4Q_FIX_ROWS;
-constexpr int UT_FIX_CHUNK = W4Q_FIX_CHUNK;  // contributors loaded together
-
+// Block (pair, ROWS rows of x); CHUNK contributors' loads go out together.
+template <int ROWS, int CHUNK>
 __global__ void __launch_bounds__(UT_PAIR_ROWS) umma_fixup_kernel(const UParams p)
 {
+    constexpr int UT_FIX_ROWS = ROWS, UT_FIX_CHUNK = CHUNK;
     // The next call's preparation may launch and wait beside these blocks
     // (measured on 6656 x 19968 at M = 16: 31.1 -> 29.4 us per call).
     pdl_launch_dependents();
@@ -628,10 +618,13 @@ __global__ void __launch_bounds__(UT_PAIR_ROWS) umma_fixup_kernel(const UParams 
         W4Q_STAMP(48);
 }
 
-cudaError_t launch_fixup(const UParams &p, cudaStream_t stream)
+cudaError_t launch_fixup(const UParams &p, int sm_count, cudaStream_t stream)
 {
+    const FixShape fs = fix_shape(p.G2, p.M, p.KB, p.U, p.P, p.split, sm_count);
+    auto fn = fs.rows == 4 ? (fs.chunk == 4 ? umma_fixup_kernel<4, 4> : umma_fixup_kernel<4, 8>)
+                           : (fs.chunk == 4 ? umma_fixup_kernel<8, 4> : umma_fixup_kernel<8, 8>);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.G2, (unsigned)((p.M + UT_FIX_ROWS - 1) / UT_FIX_ROWS));
+    cfg.gridDim = dim3((unsigned)p.G2, (unsigned)((p.M + fs.rows - 1) / fs.rows));
     cfg.blockDim = dim3(UT_PAIR_ROWS);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -639,7 +632,7 @@ cudaError_t launch_fixup(const UParams &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, umma_fixup_kernel, p);
+    return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 template <int NP>
@@ -734,7 +727,10 @@ cudaError_t launch_w4_umma(const W4Plan &plan, const void *x, const void *packed
     }
     if (e != cudaSuccess || !plan.fixup)
         return e;
-    return launch_fixup(p, stream);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return launch_fixup(p, sms, stream);
 }
 
 }  // namespace w4q

@@ -214,10 +214,6 @@ __global__ void __launch_bounds__(W8_THREADS, 1) w8_umma_kernel(const __grid_con
             int gp = gp_first, b = b_first, issued = 0;
             for (int i = 0; i < n_iter; ++i) {
                 const int slot = i % SW;
-#ifdef W4Q_UMMA_PREFETCH
-                if (i == W4Q_UMMA_PREFETCH)
-                    pdl_wait();
-#endif
                 if (i >= SW && !mbar_wait_sleep(wempty0 + 8 * slot, (uint32_t)((i / SW) - 1) & 1u)) {
                     report_error(p.err, ERR_EMPTY_WAIT);
                     break;
@@ -531,11 +527,12 @@ __global__ void __launch_bounds__(256) act_prep_w8_kernel(const __nv_bfloat16 *_
 }
 
 // Sum of the fp32 partials of the pairs that several CTAs share, in CTA
-// order, then the epilogue of the main kernel.  Block (pair, 8 rows of x).
-constexpr int W8_FIX_ROWS = 8;
-
+// order, then the epilogue of the main kernel.  Block (pair, ROWS rows of
+// x); CHUNK contributors' loads go out together.
+template <int ROWS, int CHUNK>
 __global__ void __launch_bounds__(W8_PAIR_ROWS) w8_umma_fixup_kernel(const __grid_constant__ W8UParams p)
 {
+    constexpr int W8_FIX_ROWS = ROWS;
     // The next call's preparation may launch and wait beside these blocks
     // (measured on 6656 x 19968 at M = 16: 31.1 -> 29.4 us per call).
     pdl_launch_dependents();
@@ -555,19 +552,19 @@ __global__ void __launch_bounds__(W8_PAIR_ROWS) w8_umma_fixup_kernel(const __gri
 #pragma unroll
     for (int r = 0; r < W8_FIX_ROWS; ++r)
         v[r] = (m0 + r < p.M) ? __ldcg(first + (size_t)r * W8_PAIR_ROWS) : 0.f;
-    for (int j = 0; j < nc; j += 4) {
-        float t[W8_FIX_ROWS][4];
+    for (int j = 0; j < nc; j += CHUNK) {
+        float t[W8_FIX_ROWS][CHUNK];
 #pragma unroll
         for (int r = 0; r < W8_FIX_ROWS; ++r)
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < CHUNK; ++u)
                 t[r][u] = (m0 + r < p.M && j + u < nc)
                               ? __ldcg(rest + (size_t)(j + u) * 2 * seg + (size_t)r * W8_PAIR_ROWS)
                               : 0.f;
 #pragma unroll
         for (int r = 0; r < W8_FIX_ROWS; ++r)
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < CHUNK; ++u)
                 if (j + u < nc)
                     v[r] += t[r][u];
     }
@@ -736,9 +733,12 @@ cudaError_t launch_w8_tc(const void *x, const int8_t *W, const void *scales, voi
     }
     if (e != cudaSuccess || !pl.fixup)
         return e;
-    cudaLaunchConfig_t fcfg = pdl_config(dim3((unsigned)pl.G2, (unsigned)((M + W8_FIX_ROWS - 1) / W8_FIX_ROWS)),
+    const FixShape fs = fix_shape(pl.G2, M, pl.KB, p.U, pl.P, pl.split, sm_count);
+    auto fn = fs.rows == 4 ? (fs.chunk == 4 ? w8_umma_fixup_kernel<4, 4> : w8_umma_fixup_kernel<4, 8>)
+                           : (fs.chunk == 4 ? w8_umma_fixup_kernel<8, 4> : w8_umma_fixup_kernel<8, 8>);
+    cudaLaunchConfig_t fcfg = pdl_config(dim3((unsigned)pl.G2, (unsigned)((M + fs.rows - 1) / fs.rows)),
                                          dim3(W8_PAIR_ROWS), 0, stream, attr);
-    return cudaLaunchKernelEx(&fcfg, w8_umma_fixup_kernel, p);
+    return cudaLaunchKernelEx(&fcfg, fn, p);
 }
 
 }  // namespace w4q

@@ -7,6 +7,32 @@
 
 namespace w4q {
 
+// --- partial-sum launches of the tensor-core kernels
+
+// Shape of a partial-sum launch over G2 row pairs of KB super-blocks whose
+// U units are split into P contiguous ranges (split = 0) or `split` ranges
+// per pair: rows of x per block (4 when the pairs alone would give few
+// blocks, else 8) and contributors whose loads go out together (4, or 8
+// when a pair can have more: under stream-K every range holds at least
+// floor(U / P) units, so a pair meets at most ceil((KB - 1) / floor(U / P))
+// ranges after its first).  Measured against a fixed (8, 4): 6656 x 19968
+// M = 16 29.1 -> 27.1 us, W8 8192 x 8192 M = 64 22.0 -> 21.1 us.
+struct FixShape {
+    int rows, chunk;
+};
+
+inline FixShape fix_shape(int G2, int M, int KB, long long U, int P, int split, int sm_count)
+{
+    const long long minlen = P > 0 ? U / P : 1;
+    const long long after = split > 0 ? split - 1
+                                      : (minlen > 0 ? (KB - 1 + minlen - 1) / minlen : KB);
+    FixShape fs;
+    fs.chunk = after <= 4 ? 4 : 8;
+    const long long blocks8 = (long long)G2 * ((M + 7) / 8);
+    fs.rows = blocks8 <= 2LL * (sm_count > 0 ? sm_count : 1) ? 4 : 8;
+    return fs;
+}
+
 // --- W4 pack / unpack (pack.cu)
 cudaError_t launch_pack(const void *W, void *packed, int N, int K, cudaStream_t stream);
 cudaError_t launch_unpack(const void *packed, uint8_t *q, void *scale, uint8_t *zero, int N, int K,
