@@ -639,8 +639,8 @@ template <int NP>
 cudaError_t launch_umma_np(const UParams &p, cudaStream_t stream)
 {
     auto fn = w4_umma_kernel<NP>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ut_smem<NP>());
+    static std::atomic<unsigned long long> opted_in{0};
+    cudaError_t e = smem_opt_in_once(opted_in, fn, ut_smem<NP>());
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -664,7 +664,8 @@ template <int NP>
 cudaError_t launch_w8_umma_np(const W8UParams &p, cudaStream_t stream)
 {
     auto fn = w8_umma_kernel<NP>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, w8_smem<NP>());
+    static std::atomic<unsigned long long> opted_in{0};
+    cudaError_t e = smem_opt_in_once(opted_in, fn, w8_smem<NP>());
     if (e != cudaSuccess)
         return e;
     cudaLaunchAttribute attr[1];

@@ -5,7 +5,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace w4q {
+
+// The dynamic shared-memory opt-in of kernel fn, once per device: one bit
+// per device in `done` (a device index of 64 or more opts in on every call).
+// Setting the attribute on every call cost host time on each launch.
+template <class F>
+inline cudaError_t smem_opt_in_once(std::atomic<unsigned long long> &done, F fn, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0)
+        done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // --- partial-sum launches of the tensor-core kernels
 

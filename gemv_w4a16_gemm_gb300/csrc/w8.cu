@@ -214,8 +214,8 @@ template <int M, int CH, int RW, int ST>
 cudaError_t launch_t(const W8Params &p, cudaStream_t stream)
 {
     const int smem = ST * STAGE_BYTES + CWARPS * MAX_ROWS * M * 4 + 2 * ST * 8;
-    cudaError_t e = cudaFuncSetAttribute(w8_kernel<M, CH, RW, ST>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<unsigned long long> opted_in{0};
+    cudaError_t e = smem_opt_in_once(opted_in, w8_kernel<M, CH, RW, ST>, smem);
     if (e != cudaSuccess)
         return e;
     // programmatic dependent launch: the weight stream starts while the
