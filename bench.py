@@ -220,7 +220,7 @@ class Suite:
         self.pools = {}        # (kind, N, K) -> list of weight buffers (copies)
         self.extra = {}        # (kind, N, K) -> scales (w8)
         self.x = {}            # call index -> x (device)
-        self.x_host = {}       # call index -> pinned host x
+        self.x_host = {}       # call index -> pinned host x (a view of x_host_all)
         self.out = {}          # call index -> out (device)
         self.out_host = {}
         self.ws = {}
@@ -242,12 +242,30 @@ class Suite:
                 del W
             pool = [base] + [base.clone() for _ in range(copies - 1)]
             self.pools[key] = pool
+        # Every call's x and out live in one flat buffer each (on the device
+        # and pinned on the host), at 256-byte aligned offsets, so that the
+        # end-to-end step moves its inputs and results in one copy each.
+        def offsets(sizes):
+            offs, o = [], 0
+            for n in sizes:
+                offs.append(o)
+                o += (n + 127) // 128 * 128  # bf16 elements: 256 bytes
+            return offs, o
+        x_off, x_len = offsets([M * K for _, _, K, M in self.calls])
+        o_off, o_len = offsets([M * N for _, N, _, M in self.calls])
+        self.x_host_all = torch.zeros(x_len, dtype=torch.bfloat16).pin_memory()
+        self.x_all = torch.zeros(x_len, dtype=torch.bfloat16, device=dev)
+        self.out_host_all = torch.zeros(o_len, dtype=torch.bfloat16).pin_memory()
+        self.out_all = torch.zeros(o_len, dtype=torch.bfloat16, device=dev)
         for i, (kind, N, K, M) in enumerate(self.calls):
             x = workloads.activation(M, K, seed=workloads.x_seed(N, K, M))
-            self.x_host[i] = x.pin_memory()
-            self.x[i] = x.to(dev)
-            self.out[i] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-            self.out_host[i] = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+            self.x_host[i] = self.x_host_all[x_off[i]:x_off[i] + M * K].view(M, K)
+            self.x_host[i].copy_(x)
+            self.x[i] = self.x_all[x_off[i]:x_off[i] + M * K].view(M, K)
+            self.out[i] = self.out_all[o_off[i]:o_off[i] + M * N].view(M, N)
+            self.out_host[i] = self.out_host_all[o_off[i]:o_off[i] + M * N].view(M, N)
+        self.x_all.copy_(self.x_host_all)
+        for i, (kind, N, K, M) in enumerate(self.calls):
             if kind == "w8":
                 self.ws[i] = torch.empty(max(w4q.w8_workspace_bytes(M, N, K), 16),
                                          dtype=torch.uint8, device=dev)
@@ -408,14 +426,16 @@ def run_gpu(args, rank, world, dist):
         del gi
 
     # end to end through the public API with host buffers
-    h2d = sum(suite.x_host[i].numel() * 2 for i in range(len(calls)))
-    d2h = sum(suite.out_host[i].numel() * 2 for i in range(len(calls)))
+    # one copy of every call's x in, one of every call's out back (the flat
+    # buffers, alignment padding included)
+    h2d = suite.x_host_all.numel() * 2
+    d2h = suite.out_host_all.numel() * 2
 
     def e2e_step(s):
+        suite.x_all.copy_(suite.x_host_all, non_blocking=True)
         for i in range(len(calls)):
-            suite.x[i].copy_(suite.x_host[i], non_blocking=True)
             suite.launch(i, suite.step_copy_index(i))
-            suite.out_host[i].copy_(suite.out[i], non_blocking=True)
+        suite.out_host_all.copy_(suite.out_all, non_blocking=True)
 
     for s in range(args.warmup):
         e2e_step(s)
@@ -479,7 +499,7 @@ def run_gpu(args, rank, world, dist):
         "e2e": {"value": round(world * step_weight / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "path": "eager calls of the Python binding -> C ABI, pinned host x in, out back"},
+                "path": "eager calls of the Python binding -> C ABI; every call's x in from pinned host memory in one copy, every out back in one copy"},
         "gpu_launches": suite.launches_per_step() * args.steps,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"]},
