@@ -56,6 +56,25 @@ def test_skinny_gemm_shapes(cuda, N, K):
         assert_close(out, oracle.w4a16(x, q, s, z), "N=%d K=%d M=%d" % (N, K, M))
 
 
+def test_tensor_core_split_pairs(cuda):
+    # Stream-K on the tensor core with each 256-row pair's K spread over up
+    # to 17 CTAs (2560 x 19968: 780 units over 152 CTAs), so the partial-sum
+    # launch loads its contributors in several batches.  Every output is
+    # compared (the output starts as NaN), and repeated calls agree bitwise.
+    N, K = 2560, 19968
+    W, q, s, z = quantized(N, K, seed=55)
+    packed = w4q.w4_pack_weights(W.to(cuda))
+    for M in (9, 17, 40, 64):
+        x = workloads.activation(M, K, seed=500 + M)
+        xd = x.to(cuda)
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=cuda)
+        w4q.w4a16_gemm(xd, packed, N, K, out=out)
+        assert_close(out, oracle.w4a16(x, q, s, z), "split pairs M=%d" % M)
+        for _ in range(3):
+            assert torch.equal(w4q.w4a16_gemm(xd, packed, N, K), out), M
+    assert w4q.device_error() == 0
+
+
 def test_every_legal_split_matches(cuda):
     # "test_int4_quantized_gemm.py", test_every_split_matches_dequant_matmul
     N, K = 256, 4096
