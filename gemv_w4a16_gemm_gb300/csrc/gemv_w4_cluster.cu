@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(THREADS, 2) w4_cluster_kernel(const CParams p)
                 const uint32_t sb = smem_addr(xs + i * MP * SROW);
                 const uint32_t gb = smem_addr(xg + i * MP * SROW);
                 if constexpr (MP < 8)
-                    compute_stage_packed<MP, DOTS, !A16, A16, CMP>(wbase, xb, sb, gb, zrow, lane,
+                    compute_stage_packed<MP, DOTS, !A16, A16, CMP, 1>(wbase, xb, sb, gb, zrow, lane,
                                                                    acc, p, tile, b0 + i, rs);
                 else
                     compute_stage<1, DOTS, !A16, A16, CMP>(wbase, xb, sb, gb, lane, acc, p, tile,

@@ -236,8 +236,9 @@ __device__ __forceinline__ void compute_stage(uint32_t wbase, uint32_t xbase, ui
 // 8 / MP groups side by side, and the fp32 scale / zero update runs once per
 // 8 / MP groups instead of once per group.  The lanes of one accumulator row
 // hold different slots of the same outputs; the flush adds them.  GS, SC: as
-// for compute_stage.
-template <int MP, bool DOTS, bool GS, bool SC, bool CMP = false, class PP>
+// for compute_stage.  CHAINS: accumulators a round's groups are spread over
+// (0: 4 at MP = 1, 1 above; see below).
+template <int MP, bool DOTS, bool GS, bool SC, bool CMP = false, int CHAINS = 0, class PP>
 __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xbase,
                                                      uint32_t sbase, uint32_t gbase, uint32_t zaddr,
                                                      int lane, float (&acc)[1][4], const PP &p,
@@ -262,9 +263,15 @@ __device__ __forceinline__ void compute_stage_packed(uint32_t wbase, uint32_t xb
         wv[4 * sbk + 2] = wq.z;
         wv[4 * sbk + 3] = wq.w;
     }
-    // A round's groups go to NACC accumulators (short MMA dependency chains);
-    // their columns are disjoint, so adding them afterwards is exact.
-    constexpr int NACC = GP >= 4 ? 4 : GP, GPA = GP / NACC;
+    // A round's groups go to NACC accumulators.  Their columns are disjoint
+    // (a group's MMAs add exact zeros to the other groups' columns), so one
+    // accumulator can take them all, and adding several afterwards is exact.
+    // Several give shorter MMA dependency chains, one saves the adds: at
+    // MP >= 2 the rounds already give independent chains (W4A8 39936 x 6656:
+    // M = 2 33.9 -> 32.5 us, M = 4 36.7 -> 35.8 us with one), while the
+    // stream-K kernel at MP = 1 keeps four (32.4 against 32.7 us with one).
+    constexpr int NMAX = CHAINS > 0 ? CHAINS : (MP == 1 ? 4 : 1);
+    constexpr int NACC = GP >= NMAX ? NMAX : GP, GPA = GP / NACC;
 #pragma unroll
     for (int R = 0; R < MP; ++R) {
         float dacc[NACC][4];
