@@ -48,19 +48,19 @@ WORKLOAD = "decode_linear_suite"
 # taken on: the sha256 of those files, concatenated, must still match, else
 # the roofline reports traffic as null.
 W4_SOURCES = ("gemv_w4.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
-W4_DIGEST = "96397e22497eef7f3f7ff06bc5d74380be557f9d1bc56f6299d24142ce4d2649"
+W4_DIGEST = "28b51b9b1f50293ac7cddc35fd6e60c4782a0177563e7c532fd45e7a4c405dee"
 UMMA_SOURCES = ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh", "timeline.cuh")
 UMMA_DIGEST = "d54ff4dc329a5a3302d3a0948fb19cb5c7401de19b831d97e6c7aa930a0616b8"
 CLUSTER_SOURCES = ("gemv_w4_cluster.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
-CLUSTER_DIGEST = "2e434ff71ffdcd68dee295ba6190aeb60d6c208bbf7bc27ff1af70a5c82220f3"
+CLUSTER_DIGEST = "12ba6469113f29f542150a022ed4d8ae255622d65df32f6e1a0babdf7db8ff0e"
 W8_SOURCES = ("w8.cu", "common.cuh", "timeline.cuh")
 W8_DIGEST = "3963a280236f982c48d4fee7c250e64b1b14f49dad91fbea6b562e6c9620a926"
 W8TC_SOURCES = ("gemv_w8_umma.cu", "common.cuh", "tcgen05.cuh")
 W8TC_DIGEST = "0a71e74fc9f073c78142f42130e6359bca16368c3eac45e1e902308c297c3313"
 MEASURED_TRAFFIC = {
-    "w4a8r N=39936 K=6656 M=1": (161088768, W4_SOURCES, W4_DIGEST),
-    "w4a8r N=39936 K=6656 M=4": (161192448, W4_SOURCES, W4_DIGEST),
-    "w4a16 N=6656 K=4096 M=1": (16233472, CLUSTER_SOURCES, CLUSTER_DIGEST),
+    "w4a8r N=39936 K=6656 M=1": (160875264, W4_SOURCES, W4_DIGEST),
+    "w4a8r N=39936 K=6656 M=4": (161396224, W4_SOURCES, W4_DIGEST),
+    "w4a16 N=6656 K=4096 M=1": (16232960, CLUSTER_SOURCES, CLUSTER_DIGEST),
     "w4a16 N=39936 K=6656 M=16": (161338624, UMMA_SOURCES, UMMA_DIGEST),
     "w4a16 N=39936 K=6656 M=64": (164112896, UMMA_SOURCES, UMMA_DIGEST),
     "w8 N=8192 K=8192 M=1": (67272192, W8_SOURCES, W8_DIGEST),
