@@ -54,7 +54,7 @@ UMMA_DIGEST = "d54ff4dc329a5a3302d3a0948fb19cb5c7401de19b831d97e6c7aa930a0616b8"
 CLUSTER_SOURCES = ("gemv_w4_cluster.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
 CLUSTER_DIGEST = "12ba6469113f29f542150a022ed4d8ae255622d65df32f6e1a0babdf7db8ff0e"
 W8_SOURCES = ("w8.cu", "common.cuh", "timeline.cuh")
-W8_DIGEST = "3963a280236f982c48d4fee7c250e64b1b14f49dad91fbea6b562e6c9620a926"
+W8_DIGEST = "c6e56b97f1283748b2bf5c9a038b70b960b7d278db5cb60df3b6318449743f01"
 W8TC_SOURCES = ("gemv_w8_umma.cu", "common.cuh", "tcgen05.cuh")
 W8TC_DIGEST = "0a71e74fc9f073c78142f42130e6359bca16368c3eac45e1e902308c297c3313"
 MEASURED_TRAFFIC = {
@@ -63,7 +63,7 @@ MEASURED_TRAFFIC = {
     "w4a16 N=6656 K=4096 M=1": (16232960, CLUSTER_SOURCES, CLUSTER_DIGEST),
     "w4a16 N=39936 K=6656 M=16": (161338624, UMMA_SOURCES, UMMA_DIGEST),
     "w4a16 N=39936 K=6656 M=64": (164112896, UMMA_SOURCES, UMMA_DIGEST),
-    "w8 N=8192 K=8192 M=1": (67272192, W8_SOURCES, W8_DIGEST),
+    "w8 N=8192 K=8192 M=1": (67285760, W8_SOURCES, W8_DIGEST),
     "w8 N=8192 K=8192 M=16": (67767808, W8TC_SOURCES, W8TC_DIGEST),
     "w8 N=8192 K=8192 M=64": (69326080, W8TC_SOURCES, W8TC_DIGEST),
 }
