@@ -352,10 +352,10 @@ int w8_gemv(const void *x_bf16, const int8_t *W, const void *scales_bf16,
  * positive multiple of 16 up to 2^20, N up to 2^24.
  *   workspace        device, >= w8_workspace_bytes(M, N, K) bytes, 16-byte
  *                    aligned, owned by the caller; may be NULL when that is 0
- * M = 1 with K <= 16384 runs on w8_gemv's CUDA-core kernel (no workspace;
- * measured faster there); the other calls, M = 2..4 included (measured
- * faster than w8_gemv), run on the tcgen05 tensor core in fp16 with fp32
- * accumulation: every int8 weight is an
+ * M = 1, and M = 2 with N <= 64 x (SM count), with K <= 16384 run on
+ * w8_gemv's CUDA-core kernel (no workspace; measured faster there); the
+ * other calls, M = 3..4 included (measured faster than w8_gemv), run on the
+ * tcgen05 tensor core in fp16 with fp32 accumulation: every int8 weight is an
  * fp16 number exactly, and each row m of x is scaled by a power of two
  * 2^sigma_m (max |x[m]| 2^sigma in [2^14, 2^15)), which keeps every bf16
  * value down to 2^-28 of the row's max exact in fp16; the result is

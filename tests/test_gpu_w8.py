@@ -54,7 +54,7 @@ def _check_gemm(cuda, N, K, M, seed, x=None):
     return out
 
 
-@pytest.mark.parametrize("M", (1, 4, 5, 8, 9, 16, 17, 32, 33, 48, 64))
+@pytest.mark.parametrize("M", (1, 2, 3, 4, 5, 8, 9, 16, 17, 32, 33, 48, 64))
 def test_w8_gemm_8192(cuda, M):
     # the 8192 x 8192 workload at every bucket of M (every output compared;
     # the output starts as NaN)
@@ -115,6 +115,10 @@ def test_w8_gemm_repeatable_and_workspace_checked(cuda):
     need = w4q.w8_workspace_bytes(M, N, K)
     assert need > 0 and w4q.w8_workspace_bytes(1, N, K) == 0
     assert w4q.w8_kernel_launches(1, N, K) == 1 and w4q.w8_kernel_launches(M, N, K) in (2, 3)
+    # M = 2 stays on the CUDA cores while its rows fit one wave (64 per SM)
+    sms = torch.cuda.get_device_properties(cuda).multi_processor_count
+    assert (w4q.w8_kernel_launches(2, N, K) == 1) == (N <= 64 * sms)
+    assert w4q.w8_kernel_launches(2, 64 * sms + 128, K) in (2, 3)
     ws = torch.empty(need, dtype=torch.uint8, device=cuda)
     a = w4q.w8_gemm(xd, Wd, scd, workspace=ws)
     for _ in range(3):
