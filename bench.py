@@ -50,13 +50,13 @@ WORKLOAD = "decode_linear_suite"
 W4_SOURCES = ("gemv_w4.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
 W4_DIGEST = "28b51b9b1f50293ac7cddc35fd6e60c4782a0177563e7c532fd45e7a4c405dee"
 UMMA_SOURCES = ("gemv_w4_umma.cu", "common.cuh", "tcgen05.cuh", "timeline.cuh")
-UMMA_DIGEST = "d54ff4dc329a5a3302d3a0948fb19cb5c7401de19b831d97e6c7aa930a0616b8"
+UMMA_DIGEST = "2378dafd783ae7ce4e982bd07d29ee1dc94c984069c173ab5d24492e4901e06b"
 CLUSTER_SOURCES = ("gemv_w4_cluster.cu", "w4_stage.cuh", "common.cuh", "timeline.cuh")
 CLUSTER_DIGEST = "12ba6469113f29f542150a022ed4d8ae255622d65df32f6e1a0babdf7db8ff0e"
 W8_SOURCES = ("w8.cu", "common.cuh", "timeline.cuh")
 W8_DIGEST = "c6e56b97f1283748b2bf5c9a038b70b960b7d278db5cb60df3b6318449743f01"
 W8TC_SOURCES = ("gemv_w8_umma.cu", "common.cuh", "tcgen05.cuh")
-W8TC_DIGEST = "0a71e74fc9f073c78142f42130e6359bca16368c3eac45e1e902308c297c3313"
+W8TC_DIGEST = "14fa3efbc3a7d18b41a13f47a384408feab13e645da2e80d2fc489429baf64fb"
 MEASURED_TRAFFIC = {
     "w4a8r N=39936 K=6656 M=1": (160875264, W4_SOURCES, W4_DIGEST),
     "w4a8r N=39936 K=6656 M=4": (161396224, W4_SOURCES, W4_DIGEST),

@@ -563,12 +563,12 @@ __global__ void __launch_bounds__(256) act_prep_umma_kernel(const __nv_bfloat16 
 }
 
 // Sum of the fp32 partials of the pairs that several CTAs share, in CTA
-// order (deterministic).  Block (pair, 8 rows of x), one thread per pair
-// row: every load of a group of contributors is issued before the in-order
-// sum, so the launch is about one wave of a few L2 round trips.  Launched
-// behind the main kernel with programmatic dependent launch;
-// griddepcontrol.wait holds it until the main kernel has finished.
-// Block (pair, ROWS rows of x); CHUNK contributors' loads go out together.
+// order (deterministic).  Block (pair, ROWS rows of x), one thread per pair
+// row: the loads of CHUNK contributors go out together before their
+// in-order sum, so the launch is about one wave of a few L2 round trips
+// (fix_shape picks ROWS and CHUNK).  Launched behind the main kernel with
+// programmatic dependent launch; griddepcontrol.wait holds it until the
+// main kernel has finished.
 template <int ROWS, int CHUNK>
 __global__ void __launch_bounds__(UT_PAIR_ROWS) umma_fixup_kernel(const UParams p)
 {
